@@ -1,0 +1,150 @@
+"""Python binding of libattn.so (the GB300 exact-attention library).
+
+Argument marshalling only: every function forwards to the C entry point of
+the same name declared in include/attn.h.  Pointer arguments accept torch
+tensors (their ``data_ptr()``) or plain integers; ``stream`` defaults to the
+current torch CUDA stream.  Non-zero status codes raise ``AttnError``.
+
+The library must have been built (``python -m exact_attention_77_gb300.build``);
+the first call without it raises ImportError: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_WORKSPACE = 4
+ATTN_ERR_CUDA = 5
+ATTN_ERR_TIMEOUT = 6
+ATTN_ERR_BOUNDS = 7
+
+# name -> (restype, argtypes), mirroring include/attn.h
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SIGS = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t, _P]),
+    "attn_get_device_status": (_I, [_P, ctypes.POINTER(_I)]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_exp2_probe": (_I, [_P, _P, _I, _I, _P]),
+    "attn_exp2_throughput": (_I, [_P, _I, _I, _I, _P]),
+    "attn_set_rescale_counter": (_I, [_P]),
+    "attn_set_rescale_threshold": (_I, [_F]),
+    "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: int = 0):
+        self.status = status
+        self.where = where
+        super().__init__(f"{status_string(status)} (status {status}, where {where})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is not built; run `python -m exact_attention_77_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_LIB = None
+
+
+def get_lib() -> ctypes.CDLL:
+    """The loaded libattn.so (loaded on first use; ImportError if not built)."""
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int):
+    if status != ATTN_OK:
+        raise AttnError(status)
+
+
+def status_string(status: int) -> str:
+    return get_lib().attn_status_string(status).decode()
+
+
+attn_status_string = status_string
+
+
+def attn_fwd(q, k, v, o, lse, B, H, N, d_qk, d_v, causal, scale, stream=None, check=True) -> int:
+    st = get_lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d_qk, d_v, int(causal), float(scale),
+                      _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_bwd_workspace_bytes(B, H, N, d_qk, d_v, deterministic) -> int:
+    return get_lib().attn_bwd_workspace_bytes(B, H, N, d_qk, d_v, int(deterministic))
+
+
+def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, causal, scale, deterministic, workspace,
+             workspace_bytes, stream=None, check=True) -> int:
+    st = get_lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N,
+                      d_qk, d_v, int(causal), float(scale), int(deterministic), _ptr(workspace), int(workspace_bytes),
+                      _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_get_device_status(stream=None):
+    """(status, where) after synchronising ``stream``; clears the device word."""
+    where = ctypes.c_int(0)
+    st = get_lib().attn_get_device_status(_stream(stream), ctypes.byref(where))
+    return st, where.value
+
+
+def attn_exp2_probe(x, out, n, method, stream=None):
+    _check(get_lib().attn_exp2_probe(_ptr(x), _ptr(out), n, method, _stream(stream)))
+
+
+def attn_exp2_throughput(sink, blocks, iters, method, stream=None):
+    _check(get_lib().attn_exp2_throughput(_ptr(sink), blocks, iters, method, _stream(stream)))
+
+
+def attn_set_rescale_counter(counter):
+    _check(get_lib().attn_set_rescale_counter(_ptr(counter)))
+
+
+def attn_set_rescale_threshold(tau: float):
+    _check(get_lib().attn_set_rescale_threshold(float(tau)))
+
+
+def attn_selftest_wait_timeout(timeout_us: int, stream=None):
+    _check(get_lib().attn_selftest_wait_timeout(int(timeout_us), _stream(stream)))

@@ -1,0 +1,298 @@
+// C ABI of the library: argument checks, TMA descriptors, workspace layout,
+// kernel selection and launch, and the device status word.  No device
+// allocation happens here; the caller owns every buffer.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "attn.h"
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace attn {
+cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
+cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
+cudaError_t launch_fwd_d192(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
+cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s);
+cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s);
+}  // namespace attn
+
+__device__ attn::DeviceStatus g_attn_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct Settings {
+  unsigned long long timeout_ns = 5ull * 1000 * 1000 * 1000;
+  int fwd_tiles = 2;  // query tiles per forward CTA (d = 64 / 128)
+  int fwd_poly = 1;   // polynomial share of the exponentials on
+  float tau = 8.0f;
+  unsigned long long* rescale_counter = nullptr;
+};
+
+std::mutex g_mu;
+Settings g_settings;
+bool g_env_read = false;
+attn::DeviceStatus* g_status_ptr[kMaxDevices] = {nullptr};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+Settings settings() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_env_read) {
+    g_env_read = true;
+    if (const char* e = getenv("ATTN_TIMEOUT_MS")) {
+      const long ms = atol(e);
+      if (ms > 0) g_settings.timeout_ns = (unsigned long long)ms * 1000000ull;
+    }
+    if (const char* e = getenv("ATTN_FWD_TILES")) {
+      const int v = atoi(e);
+      if (v == 1 || v == 2) g_settings.fwd_tiles = v;
+    }
+    if (const char* e = getenv("ATTN_EXP_POLY")) g_settings.fwd_poly = atoi(e) != 0;
+  }
+  return g_settings;
+}
+
+// Device status word of the current device (resolved once per device).
+int status_ptr(attn::DeviceStatus** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return ATTN_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<attn::DeviceStatus*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return ATTN_OK;
+}
+
+int encoder(EncodeTiledFn* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = g_encode;
+  return ATTN_OK;
+}
+
+// 3-D view [BH, N, d] of a contiguous bf16 tensor; box 64 (d) x 128 (rows) x 1
+// with the 128-byte swizzle; rows past N read as zero.
+int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+  EncodeTiledFn enc;
+  if (int st = encoder(&enc)) return st;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int N, float scale, int causal) {
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * H >= (1ll << 31) || N >= (1 << 24)) return ATTN_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+bool fwd_dims_ok(int d_qk, int d_v) {
+  return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 192 && d_v == 128);
+}
+
+bool bwd_dims_ok(int d_qk, int d_v) { return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128); }
+
+struct WorkspaceLayout {
+  size_t lse2, d, acc, tickets, total;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WorkspaceLayout workspace_layout(int B, int H, int N, int d_qk, int deterministic) {
+  WorkspaceLayout w;
+  const size_t bh = (size_t)B * H;
+  const size_t tiles = ((size_t)N + 127) / 128;
+  const size_t npad = tiles * 128;
+  w.lse2 = 0;
+  w.d = round_up(w.lse2 + bh * npad * 4, 256);
+  w.acc = round_up(w.d + bh * npad * 4, 256);
+  w.tickets = round_up(w.acc + bh * npad * (size_t)d_qk * 4, 256);
+  w.total = round_up(w.tickets + (deterministic ? bh * tiles * 4 : 0), 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_BOUNDS: return "ATTN_ERR_BOUNDS";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+int attn_set_rescale_counter(unsigned long long* counter) {
+  settings();
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_settings.rescale_counter = counter;
+  return ATTN_OK;
+}
+
+int attn_set_rescale_threshold(float tau) {
+  if (!isfinite(tau) || tau < 0.f || tau > 16.f) return ATTN_ERR_INVALID_ARG;
+  settings();
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_settings.tau = tau;
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d_qk,
+             int d_v, int causal, float scale, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (int st = check_common(B, H, N, scale, causal)) return st;
+  if (!fwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  const Settings cfg = settings();
+  attn::FwdParams p;
+  memset(&p, 0, sizeof(p));
+  const int BH = B * H;
+  if (int st = make_map(&p.tm_q, q, BH, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_k, k, BH, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_v, v, BH, N, d_v)) return st;
+  if (int st = status_ptr(&p.status)) return st;
+  p.o = o;
+  p.lse = lse;
+  p.rescale_counter = cfg.rescale_counter;
+  p.timeout_ns = cfg.timeout_ns;
+  p.N = N;
+  p.BH = BH;
+  p.n_qtiles = (N + 127) / 128;
+  const int nqt = d_qk == 192 ? 2 : cfg.fwd_tiles;
+  p.n_blocks = BH * ((p.n_qtiles + nqt - 1) / nqt);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.tau = cfg.tau;
+  cudaError_t e;
+  if (d_qk == 64) e = attn::launch_fwd_d64(p, causal != 0, nqt, cfg.fwd_poly, stream);
+  else if (d_qk == 128) e = attn::launch_fwd_d128(p, causal != 0, nqt, cfg.fwd_poly, stream);
+  else e = attn::launch_fwd_d192(p, causal != 0, nqt, cfg.fwd_poly, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d_qk, int d_v, int deterministic) {
+  if (check_common(B, H, N, 1.0f, 0) != ATTN_OK || !bwd_dims_ok(d_qk, d_v)) return 0;
+  if (deterministic != 0 && deterministic != 1) return 0;
+  return workspace_layout(B, H, N, d_qk, deterministic).total;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale,
+             int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (int st = check_common(B, H, N, scale, causal)) return st;
+  if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
+  if (!bwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return ATTN_ERR_MISALIGNED;
+  const WorkspaceLayout w = workspace_layout(B, H, N, d_qk, deterministic);
+  if (workspace == nullptr || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  const Settings cfg = settings();
+  attn::BwdParams p;
+  memset(&p, 0, sizeof(p));
+  const int BH = B * H;
+  if (int st = make_map(&p.tm_q, q, BH, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_k, k, BH, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_v, v, BH, N, d_v)) return st;
+  if (int st = make_map(&p.tm_do, dO, BH, N, d_v)) return st;
+  if (int st = status_ptr(&p.status)) return st;
+  char* ws = static_cast<char*>(workspace);
+  p.o = o;
+  p.dO = dO;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.row_lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  p.row_d = reinterpret_cast<float*>(ws + w.d);
+  p.dq_acc = reinterpret_cast<float*>(ws + w.acc);
+  p.tickets = deterministic ? reinterpret_cast<int*>(ws + w.tickets) : nullptr;
+  p.timeout_ns = cfg.timeout_ns;
+  p.N = N;
+  p.n_tiles = (N + 127) / 128;
+  p.Npad = p.n_tiles * 128;
+  p.BH = BH;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = d_qk == 64 ? attn::launch_bwd_d64(p, causal != 0, deterministic != 0, stream)
+                             : attn::launch_bwd_d128(p, causal != 0, deterministic != 0, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_get_device_status(cudaStream_t stream, int* where) {
+  if (where) *where = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  attn::DeviceStatus* dev_status;
+  if (int st = status_ptr(&dev_status)) return st;
+  attn::DeviceStatus host{0, 0};
+  if (cudaMemcpy(&host, dev_status, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (host.code != 0) {
+    const attn::DeviceStatus zero{0, 0};
+    if (cudaMemcpy(dev_status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  if (where) *where = host.where;
+  return host.code;
+}
+
+int attn_exp2_probe(const float* x, float* out, int n, int method, cudaStream_t stream) {
+  if (!x || !out || n < 0) return ATTN_ERR_INVALID_ARG;
+  if (method != 0 && method != 3 && method != 4 && method != 5) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return ATTN_OK;
+  return attn::launch_exp2_probe(x, out, n, method, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_exp2_throughput(float* sink, int blocks, int iters, int method, cudaStream_t stream) {
+  if (!sink || blocks < 1 || iters < 1) return ATTN_ERR_INVALID_ARG;
+  if (method != 0 && method != 3 && method != 4 && method != 5) return ATTN_ERR_INVALID_ARG;
+  return attn::launch_exp2_throughput(sink, blocks, iters, method, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream) {
+  if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return ATTN_ERR_INVALID_ARG;
+  attn::DeviceStatus* st;
+  if (int e = status_ptr(&st)) return e;
+  return attn::launch_wait_selftest(st, (unsigned long long)timeout_us * 1000ull, stream) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,505 @@
+// Backward attention kernels for sm_103a (templates; instantiated per head dim
+// in attn_bwd_d*.cu).
+//
+// What they compute: dQ, dK, dV of L = sum(O * dO) for O = softmax(S) V,
+// S = scale Q K^T (+ causal mask).  With P recomputed from the saved LSE,
+// D_i = dO_i . O_i and dS = P o (dP - D), dP = dO V^T:
+//     dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K.
+// "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for Asymmetric
+// Hardware Scaling", Figure 2 and Table 3, describe this graph of five
+// products and two elementwise steps; the abstract and Figures 7-8 the atomic
+// and the deterministic accumulation of dQ.
+//
+// Kernels:
+//   bwd_pre_kernel   D_i = rowsum(dO o O) and LSE_i * log2(e) into the
+//                    workspace (padding rows: D = 0, LSE2 = +inf so P = 0);
+//                    zeroes the FP32 dQ accumulator and the tickets.
+//   bwd_kernel       one CTA per (b, h, 128-key tile j), K_j and V_j resident;
+//                    for each query tile i it runs, with keys on the tensor-
+//                    memory lanes:
+//                      S^T  = K_j Q_i^T          (SS)
+//                      dP^T = V_j dO_i^T         (SS)
+//                      P^T  = 2^(S^T*scale*log2e - LSE2_i), dS^T = P^T o (dP^T - D_i)
+//                      dV  += P^T dO_i           (TS, P^T bf16 in tensor memory)
+//                      dK  += dS^T Q_i           (TS, dS^T bf16 in tensor memory)
+//                      dQ_i = dS K_j             (SS, dS bf16 in shared memory)
+//                    and adds dQ_i into the FP32 accumulator with bulk
+//                    reduce-add copies (atomic mode), or in ascending-j order
+//                    behind a per-(b, h, i) ticket (deterministic mode).
+//   dq_convert_kernel  dQ = scale * accumulator, as bf16 [B,H,N,d].
+//
+// Warp roles in bwd_kernel (320 threads): warp 0 producer (TMA), warp 1 MMA
+// issuer and tensor-memory owner, warps 2-5 the elementwise warpgroup (one
+// key row per thread), warps 6-9 the dQ warpgroup (one query row per thread).
+#pragma once
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace attn {
+
+constexpr int kBTile = 128;
+constexpr int kBSub = 128 * 128;  // 128 rows x 128 bytes
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kTileBytes = kBTile * D * 2;  // one bf16 [128, D] tile
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTileBytes;
+  static constexpr int kQOff = kVOff + kTileBytes;           // 2 stages
+  static constexpr int kDOOff = kQOff + 2 * kTileBytes;      // 2 stages
+  static constexpr int kDSOff = kDOOff + 2 * kTileBytes;     // dS (bf16 128x128) / dQ staging
+  static constexpr int kDSBytes = kBTile * kBTile * 2;
+  static constexpr int kVecOff = kDSOff + kDSBytes;          // 2 stages x (LSE2[128], D[128]) fp32
+  static constexpr int kVecBytes = 2 * kBTile * 4;
+  static constexpr int kBarOff = kVecOff + 2 * kVecBytes;
+  enum {
+    kBarKV = 0,
+    kBarQFull = 1,   // +stage
+    kBarQEmpty = 3,
+    kBarDOFull = 5,
+    kBarDOEmpty = 7,
+    kBarSFull = 9,
+    kBarDPFull,
+    kBarDSFull,
+    kBarDQFull,
+    kBarDQFree,
+    kBarDSFree,
+    kBarAccDone,
+    kNumBars
+  };
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  // tensor memory columns
+  static constexpr int kColS = 0;      // S^T fp32 [128 x 128]; P^T bf16 in its first 64 columns
+  static constexpr int kColDP = 128;   // dP^T fp32; dS^T bf16 in its first 64 columns
+  static constexpr int kColDV = 256;   // dV accumulator [128 x D]
+  static constexpr int kColDK = 256 + D;
+  static constexpr int kColDQ = D == 64 ? 384 : 0;  // d = 128 shares the S^T columns
+  static constexpr int kThreads = 320;
+};
+
+enum : int {
+  kBWhereProd = 110, kBWhereMma = 120, kBWhereEw = 130, kBWhereDq = 140, kBWhereTicket = 141, kBWhereFin = 150
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// -------------------------------------------------------------- preprocess
+// One group of D/8 lanes per row, 16-byte loads.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(BwdParams p) {
+  constexpr int kLanes = D / 8;
+  constexpr int kRowsPerBlock = 256 / kLanes;
+  const int sub = threadIdx.x % kLanes;
+  const long row = (long)blockIdx.x * kRowsPerBlock + threadIdx.x / kLanes;  // over BH * Npad
+  const long total_rows = (long)p.BH * p.Npad;
+  const bool in_range = row < total_rows;
+  const int bh = in_range ? (int)(row / p.Npad) : 0;
+  const int i = in_range ? (int)(row - (long)bh * p.Npad) : p.N;
+  float acc = 0.f;
+  if (i < p.N) {
+    const size_t off = ((size_t)bh * p.N + i) * D + sub * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dO) + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 fa = __bfloat1622float2(a2[k]);
+      const float2 fb = __bfloat1622float2(b2[k]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, kLanes);
+  if (in_range && sub == 0) {
+    p.row_d[row] = acc;
+    p.row_lse2[row] = i < p.N ? p.lse[(size_t)bh * p.N + i] * 1.4426950408889634f : INFINITY;
+  }
+  // zero the dQ accumulator and the tickets (grid-stride, 16-byte stores)
+  const size_t n4 = (size_t)p.BH * p.Npad * D / 4;
+  float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
+  for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += (size_t)gridDim.x * blockDim.x)
+    acc4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (p.tickets != nullptr)
+    for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < (size_t)p.BH * p.n_tiles;
+         k += (size_t)gridDim.x * blockDim.x)
+      p.tickets[k] = 0;
+}
+
+// ---------------------------------------------------------------- dQ out
+// Accumulator layout per (bh, tile): [D/4 groups][128 rows][4]; one warp per
+// row, lane g handles columns 4g..4g+3 (D = 128) or two lanes share (D = 64).
+template <int D>
+__global__ void __launch_bounds__(256) dq_convert_kernel(BwdParams p) {
+  constexpr int kGroups = D / 4;                 // 32 or 16
+  constexpr int kRowsPerWarp = 32 / kGroups;      // 1 or 2
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long row = (long)warp * kRowsPerWarp + lane / kGroups;
+  const int g = lane % kGroups;
+  if (row >= (long)p.BH * p.N) return;
+  const int bh = (int)(row / p.N);
+  const int i = (int)(row - (long)bh * p.N);
+  const int tile = i >> 7, r = i & 127;
+  const float4 a = *reinterpret_cast<const float4*>(
+      p.dq_acc + ((((size_t)bh * p.n_tiles + tile) * kGroups + g) * 128 + r) * 4);
+  uint2 out;
+  out.x = pack_bf16(a.x * p.scale, a.y * p.scale);
+  out.y = pack_bf16(a.z * p.scale, a.w * p.scale);
+  *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + (size_t)row * D + 4 * g) = out;
+}
+
+// ---------------------------------------------------------------- main
+template <int D, bool CAUSAL, bool DETERMINISTIC>
+__global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) report_error(p.status, ATTN_ERR_BOUNDS, 2);
+    return;
+  }
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  // work unit: key tile j of head bh; key-tile-major so that the CTAs a
+  // deterministic CTA waits for (smaller j, same head) were launched first,
+  // and (causal) the longest columns go first.
+  const int n = p.n_tiles;
+  const int j = blockIdx.x / p.BH;
+  const int bh = blockIdx.x - j * p.BH;
+  const int i_lo = CAUSAL ? j : 0;  // query tiles i_lo .. n-1, visited from n-1 down
+  const int n_it = n - i_lo;
+  auto tile_of = [&](int it) { return n - 1 - it; };
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < L::kNumBars; ++b) {
+      uint32_t cnt = 1;
+      if (b == L::kBarDSFull || b == L::kBarDQFree) cnt = 128;
+      mbar_init(bar(b), cnt);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ============================ producer ============================
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_q);
+      prefetch_tensormap(&p.tm_k);
+      prefetch_tensormap(&p.tm_v);
+      prefetch_tensormap(&p.tm_do);
+      mbar_arrive_expect_tx(bar(L::kBarKV), 2 * L::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sbase + L::kKOff + c * kBSub, &p.tm_k, c * 64, j * kBTile, bh, bar(L::kBarKV));
+        tma_load_3d(sbase + L::kVOff + c * kBSub, &p.tm_v, c * 64, j * kBTile, bh, bar(L::kBarKV));
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = ((it >> 1) & 1) ^ 1;
+        const int i = tile_of(it);
+        if (!mbar_wait(bar(L::kBarQEmpty + s), ph, ctl, kBWhereProd)) break;
+        mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kTileBytes + L::kVecBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sbase + L::kQOff + s * L::kTileBytes + c * kBSub, &p.tm_q, c * 64, i * kBTile, bh,
+                      bar(L::kBarQFull + s));
+        const size_t vrow = (size_t)bh * p.Npad + (size_t)i * kBTile;
+        bulk_load(sbase + L::kVecOff + s * L::kVecBytes, p.row_lse2 + vrow, kBTile * 4, bar(L::kBarQFull + s));
+        bulk_load(sbase + L::kVecOff + s * L::kVecBytes + kBTile * 4, p.row_d + vrow, kBTile * 4,
+                  bar(L::kBarQFull + s));
+        if (!mbar_wait(bar(L::kBarDOEmpty + s), ph, ctl, kBWhereProd + 1)) {
+          issued = it + 1;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(L::kBarDOFull + s), L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sbase + L::kDOOff + s * L::kTileBytes + c * kBSub, &p.tm_do, c * 64, i * kBTile, bh,
+                      bar(L::kBarDOFull + s));
+        issued = it + 1;
+      }
+      mbar_wait_drain(bar(L::kBarKV), 0, p.timeout_ns);
+      for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it) {
+        mbar_wait_drain(bar(L::kBarQFull + (it & 1)), (it >> 1) & 1, p.timeout_ns);
+        mbar_wait_drain(bar(L::kBarDOFull + (it & 1)), (it >> 1) & 1, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ===========================
+    if (lane == 0) {
+      constexpr uint32_t kIdSq = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);    // dV, dK (A in tensor memory)
+      constexpr uint32_t kIdDq = idesc_bf16_f32(128, D, true, true);      // dQ (A = dS, MN-major)
+      // C = A B with A [128 x D] K-major at a_base and B [128 x D] K-major at b_base
+      auto mma_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kBSub + (kk % 4) * 32;
+          mma_ss(tmem + d_col, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), kIdSq,
+                 kk > 0);
+        }
+      };
+      // C (+)= A[tmem, 128 x 128 bf16] B, B = [128 (K) x D] MN-major at b_base
+      auto mma_tmem_a = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBTile / 16; ++kk)
+          mma_ts(tmem + d_col, tmem + a_col + kk * 8, sdesc_sw128(b_base + kk * 2048, kBSub, 1024), kIdAcc,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar(L::kBarKV), 0, ctl, kBWhereMma);
+      tc_fence_after();
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        const uint32_t qs = sbase + L::kQOff + s * L::kTileBytes;
+        const uint32_t dos = sbase + L::kDOOff + s * L::kTileBytes;
+        if (!(ok = mbar_wait(bar(L::kBarQFull + s), ph, ctl, kBWhereMma + 1))) break;
+        if (L::kColDQ == L::kColS && it > 0)  // S^T columns still hold dQ of the previous tile
+          if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 2))) break;
+        tc_fence_after();
+        mma_kmajor(L::kColS, sbase + L::kKOff, qs);
+        tc_commit(bar(L::kBarSFull));
+        if (!(ok = mbar_wait(bar(L::kBarDOFull + s), ph, ctl, kBWhereMma + 3))) break;
+        tc_fence_after();
+        mma_kmajor(L::kColDP, sbase + L::kVOff, dos);
+        tc_commit(bar(L::kBarDPFull));
+        if (!(ok = mbar_wait(bar(L::kBarDSFull), it & 1, ctl, kBWhereMma + 4))) break;
+        tc_fence_after();
+        mma_tmem_a(L::kColDV, L::kColS, dos, it > 0);
+        mma_tmem_a(L::kColDK, L::kColDP, qs, it > 0);
+        tc_commit(bar(L::kBarQEmpty + s));
+        tc_commit(bar(L::kBarDOEmpty + s));
+        if (L::kColDQ != L::kColS && it > 0)
+          if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 5))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBTile / 16; ++kk)
+          mma_ss(tmem + L::kColDQ, sdesc_sw128(sbase + L::kDSOff + kk * 2048, kBSub, 1024),
+                 sdesc_sw128(sbase + L::kKOff + kk * 2048, kBSub, 1024), kIdDq, kk > 0);
+        tc_commit(bar(L::kBarDQFull));
+      }
+      tc_commit(bar(L::kBarAccDone));
+      mbar_wait_drain(bar(L::kBarAccDone), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ======================= elementwise warpgroup ======================
+    const int quad = warp & 3;
+    const int krow = quad * 32 + lane;  // key row within the tile (tensor-memory lane)
+    const int k_glob = j * kBTile + krow;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + L::kColS;
+    const uint32_t tDP = tmem + lane_base + L::kColDP;
+    const float c_log2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1;
+      const int i = tile_of(it);
+      // the stage's LSE2 / D vectors arrive with Q_i on the same barrier
+      ok = mbar_wait(bar(L::kBarQFull + s), (it >> 1) & 1, ctl, kBWhereEw + 3);
+      ok = ok && mbar_wait(bar(L::kBarSFull), it & 1, ctl, kBWhereEw);
+      ok = ok && mbar_wait(bar(L::kBarDPFull), it & 1, ctl, kBWhereEw + 1);
+      // the dS buffer doubles as dQ staging: wait until its bulk reads are done
+      ok = ok && (it == 0 || mbar_wait(bar(L::kBarDSFree), (it - 1) & 1, ctl, kBWhereEw + 2));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* vec = reinterpret_cast<const float*>(smem + L::kVecOff + s * L::kVecBytes);
+      const bool diag = CAUSAL && i == j;
+      const bool key_dead = k_glob >= p.N;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kBTile; c0 += 32) {
+        float sv[32], dp[32];
+        tmem_ld32(tS + c0, sv);
+        tmem_ld32(tDP + c0, dp);
+        uint32_t pk[16], dk[16];
+        float dsv[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int qi = c0 + q;
+          float pv = ex2_mufu(fmaf(sv[q], c_log2, -vec[qi]));
+          if (key_dead || (diag && (i * kBTile + qi) < k_glob)) pv = 0.f;
+          const float ds = pv * (dp[q] - vec[kBTile + qi]);
+          dsv[q] = ds;
+          sv[q] = pv;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          pk[q] = pack_bf16(sv[2 * q], sv[2 * q + 1]);
+          dk[q] = pack_bf16(dsv[2 * q], dsv[2 * q + 1]);
+        }
+        tmem_st16(tS + c0 / 2, pk);
+        tmem_st16(tDP + c0 / 2, dk);
+        // dS (queries x keys) into shared memory, MN-major with the 128-byte
+        // swizzle: query chunk (c0/64) at 16 KB, key row krow at
+        // (krow/8)*1024 + (krow%8)*128, 16-byte unit (q%64)/8 xor (krow%8).
+        uint8_t* ds_base = smem + L::kDSOff + (c0 / 64) * kBSub + (krow >> 3) * 1024 + (krow & 7) * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = ((c0 % 64) / 8 + u) ^ (krow & 7);
+          *reinterpret_cast<uint4*>(ds_base + unit * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDSFull));
+    }
+    // epilogue: dV, dK rows of this key tile
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, ctl, kBWhereFin));
+    if (ok) {
+      tc_fence_after();
+      const bool live = k_glob < p.N;
+      const size_t row = (size_t)bh * p.N + (live ? k_glob : 0);
+      uint4* dvrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dv) + row * D);
+      uint4* dkrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dk) + row * D);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float a[32], b[32];
+        tmem_ld32(tmem + lane_base + L::kColDV + c0, a);
+        tmem_ld32(tmem + lane_base + L::kColDK + c0, b);
+        uint32_t pa[16], pb[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          pa[q] = pack_bf16(a[2 * q], a[2 * q + 1]);
+          pb[q] = pack_bf16(b[2 * q] * p.scale, b[2 * q + 1] * p.scale);
+        }
+        if (live) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            dvrow[c0 / 8 + v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
+            dkrow[c0 / 8 + v] = make_uint4(pb[4 * v], pb[4 * v + 1], pb[4 * v + 2], pb[4 * v + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // =========================== dQ warpgroup ===========================
+    const int quad = warp & 3;
+    const int qrow = quad * 32 + lane;  // query row within the tile (tensor-memory lane)
+    const int tid = threadIdx.x - 192;  // 0..127 within the warpgroup
+    const uint32_t tDQ = tmem + ((uint32_t)(quad * 32) << 16) + L::kColDQ;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int i = tile_of(it);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
+      if (!ok) break;
+      tc_fence_after();
+      float dq[D];
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32p(tDQ + c0, dq + c0);
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDQFree));  // tensor-memory dQ columns may be overwritten
+      // stage through the dS buffer (its last reader, the dQ product, is done)
+      // in [column group][row][4] order, 16 KB (32 columns) per bulk reduction
+      float* gdst = p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile);
+      if (DETERMINISTIC && tid == 0) {
+        const int* tk = p.tickets + (size_t)bh * p.n_tiles + i;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(tk) != j) {  // tile i takes key tiles in ascending j
+          if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
+            if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
+            *ctl.abort = 1;
+            break;
+          }
+        }
+        fence_proxy_async_global();
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        const int buf = c & 1;
+        if (c >= 2) {
+          if (tid == 0) bulk_wait_read<1>();
+          named_bar_sync(1, 128);
+        }
+        float* st = reinterpret_cast<float*>(smem + L::kDSOff + buf * 16384);
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<float4*>(st + (g * 128 + qrow) * 4) =
+              make_float4(dq[c * 32 + 4 * g], dq[c * 32 + 4 * g + 1], dq[c * 32 + 4 * g + 2], dq[c * 32 + 4 * g + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (tid == 0 && !*ctl.abort) {
+          bulk_reduce_add_f32(gdst + (size_t)c * 32 * kBTile, smem_u32(st), 16384);
+          bulk_commit();
+        }
+      }
+      if (tid == 0) {
+        if (DETERMINISTIC) {
+          bulk_wait_all<0>();
+          fence_proxy_async_global();
+          if (!*ctl.abort) red_release_gpu_add(p.tickets + (size_t)bh * p.n_tiles + i, 1);
+        } else {
+          bulk_wait_read<0>();
+        }
+        mbar_arrive(bar(L::kBarDSFree));  // the dS buffer may be rewritten
+      }
+      __syncwarp();
+    }
+    if (tid == 0) bulk_wait_all<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool DET>
+cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  // preprocess: D, LSE2, zeroed accumulator / tickets
+  {
+    const long rows = (long)p.BH * p.Npad;
+    const int rows_per_block = 256 / (D / 8);
+    const long blocks = (rows + rows_per_block - 1) / rows_per_block;
+    bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kernel = bwd_kernel<D, CAUSAL, DET>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kernel<<<p.BH * p.n_tiles, L::kThreads, L::kSmemBytes, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const long warps = ((long)p.BH * p.N + (32 / (D / 4)) - 1) / (32 / (D / 4));
+    const long blocks = (warps * 32 + 255) / 256;
+    dq_convert_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace attn

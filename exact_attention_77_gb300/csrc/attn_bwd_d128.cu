@@ -1,0 +1,11 @@
+// Backward kernel instances for d_qk = d_v = 128.
+#include "attn_bwd.cuh"
+
+namespace attn {
+
+cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s) {
+  if (causal) return deterministic ? launch_bwd_instance<128, true, true>(p, s) : launch_bwd_instance<128, true, false>(p, s);
+  return deterministic ? launch_bwd_instance<128, false, true>(p, s) : launch_bwd_instance<128, false, false>(p, s);
+}
+
+}  // namespace attn

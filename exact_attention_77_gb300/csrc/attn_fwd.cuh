@@ -1,0 +1,411 @@
+// Forward attention kernel for sm_103a (template; instantiated per head dim in
+// attn_fwd_d*.cu).
+//
+// What it computes: O = softmax(scale Q K^T + causal mask) V and the per-row
+// natural-log LSE, with the score matrix kept on chip ("Attention at Scale --
+// From FlashAttention to FlashAttention-4", sections "The Problem" and "The
+// Evolution"), the online softmax with conditional rescaling ("FlashAttention
+// 3 and 4: When the Bottleneck Moves", section 3.2), and the exponentials split
+// between the hardware unit and a polynomial (same section; "FlashAttention-4:
+// Algorithm and Kernel Pipelining Co-Design for Asymmetric Hardware Scaling",
+// abstract and Table 2).
+//
+// CTA structure (one CTA = NQT query tiles of 128 rows of one (b, h)):
+//   warp 0      producer: TMA loads of the Q tiles, then K_j / V_j tiles into a
+//               ring of shared-memory stages behind full/empty mbarriers;
+//   warp 1      owns tensor memory; one thread issues every tcgen05.mma:
+//               S_t = Q_t K_j^T (both operands K-major in shared memory) and
+//               O_t += P_t V_j (P_t from tensor memory, V_j MN-major);
+//   warps 2-3   idle (the first warpgroup hands its registers to the others);
+//   warps 4..   one warpgroup per query tile: thread r owns row r of the tile,
+//               loads its 128 scores from tensor memory, takes the row max,
+//               rescales O_t and l only when the max rose by more than tau,
+//               forms P = 2^(S*scale*log2e - m) in FP32 and writes it back as
+//               bf16 over the first 64 columns of S_t, then normalises once at
+//               the end.
+// With two query tiles the issue order S_0(j+1) .. PV_1(j) .. S_1(j+1) lets one
+// tile's softmax overlap the other tile's products ("FlashAttention-4 ...",
+// Figure 1).  Tensor memory per query tile: S (128 columns) then O (d_v).
+//
+// Every wait is bounded (see sm103.cuh): on a timeout the kernel records
+// ATTN_ERR_TIMEOUT, every role stops, in-flight copies and products are
+// drained, tensor memory is released and the CTA exits.
+#pragma once
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace attn {
+
+constexpr int kTile = 128;
+constexpr int kSubTile = 128 * 128;  // bytes: 128 rows x 64 bf16 (one 128-byte swizzle span)
+// Of every 32 score columns, this many take the polynomial exponential and the
+// rest the hardware unit (the "poly" kernel variants; 0 = hardware only).
+constexpr int kPolyCols = 10;
+
+template <int DQK, int DV, int NQT>
+struct FwdLayout {
+  static constexpr int kQBytes = kTile * DQK * 2;
+  static constexpr int kKBytes = kTile * DQK * 2;
+  static constexpr int kVBytes = kTile * DV * 2;
+  static constexpr int kStageBytes = kKBytes > kVBytes ? kKBytes : kVBytes;
+  static constexpr int kQRegion = NQT * kQBytes;
+  // One query tile per CTA is sized so two CTAs share an SM (two softmax
+  // warpgroups per SM either way); two tiles take the SM alone.
+  static constexpr int kBudget = NQT == 1 ? 110 * 1024 : 226 * 1024;
+  static constexpr int kStagesFit = (kBudget - kQRegion) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
+  static_assert(kStages >= 2, "K/V ring needs two stages");
+  static constexpr int kThreads = 128 + 128 * NQT;
+  static constexpr int kMinBlocks = NQT == 1 ? 2 : 1;
+  // Register split (setmaxnreg): the launch gives every thread kLaunchRegs;
+  // the control warpgroup drops to kCtlRegs and each softmax warpgroup rises
+  // to kSmRegs.  kCtlRegs * 128 + kSmRegs * 128 * NQT == kLaunchRegs * kThreads.
+  static constexpr int kLaunchRegs = NQT == 1 ? 128 : 168;
+  static constexpr int kCtlRegs = NQT == 1 ? 40 : 56;
+  static constexpr int kSmRegs = NQT == 1 ? 216 : 224;
+  static_assert(kCtlRegs * 128 + kSmRegs * 128 * NQT == kLaunchRegs * kThreads, "register split");
+  static constexpr int kKVOff = kQRegion;
+  static constexpr int kBarOff = kKVOff + kStages * kStageBytes;
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarKVFull = 1;
+  static constexpr int kBarKVEmpty = kBarKVFull + kStages;
+  static constexpr int kBarSFull = kBarKVEmpty + kStages;
+  static constexpr int kBarPFull = kBarSFull + NQT;
+  static constexpr int kBarODone = kBarPFull + NQT;
+  static constexpr int kBarMmaDone = kBarODone + NQT;
+  static constexpr int kNumBars = kBarMmaDone + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  // Tensor memory decides residency: two CTAs of 256 columns per SM, or one of
+  // 512.  The shared-memory request is padded so no extra CTA lands on an SM
+  // only to wait in tcgen05.alloc.
+  static constexpr int kSmemMin = NQT == 1 ? 80 * 1024 : 116 * 1024;
+  static constexpr int kSmemBytes = kMiscOff + 16 > kSmemMin ? kMiscOff + 16 : kSmemMin;
+  static constexpr int kTmemCols = NQT == 1 ? 256 : 512;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+// Where-codes recorded with a timeout (role * 10 + wait).
+enum : int {
+  kWhereProdEmpty = 10, kWhereMmaQ = 20, kWhereMmaKV = 21, kWhereMmaP = 22,
+  kWhereSmS = 30, kWhereSmO = 31, kWhereSmFinal = 32, kWhereAlign = 1
+};
+
+template <int DQK, int DV, int NQT, bool CAUSAL, int POLY>
+__global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<DQK, DV, NQT>::kMinBlocks)
+    fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = FwdLayout<DQK, DV, NQT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // swizzled operand tiles need 1024-byte alignment
+    if (threadIdx.x == 0) report_error(p.status, ATTN_ERR_BOUNDS, kWhereAlign);
+    return;
+  }
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  // ---- work unit: (bh, block of NQT query tiles)
+  const int n_qblocks = (p.n_qtiles + NQT - 1) / NQT;
+  int bh, qblock;
+  if (CAUSAL) {  // longest rows first, spread over heads
+    const int rank = blockIdx.x / p.BH;
+    bh = blockIdx.x - rank * p.BH;
+    qblock = n_qblocks - 1 - rank;
+  } else {  // head-major keeps one head's K/V hot in L2
+    bh = blockIdx.x / n_qblocks;
+    qblock = blockIdx.x - bh * n_qblocks;
+  }
+  int nkv[NQT];
+  int nkv_max = 0;
+#pragma unroll
+  for (int t = 0; t < NQT; ++t) {
+    const int qt = qblock * NQT + t;
+    nkv[t] = qt < p.n_qtiles ? (CAUSAL ? qt + 1 : p.n_qtiles) : 0;
+    nkv_max = nkv[t] > nkv_max ? nkv[t] : nkv_max;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kBarQFull), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar(L::kBarKVFull + s), 1);
+      mbar_init(bar(L::kBarKVEmpty + s), 1);
+    }
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(bar(L::kBarSFull + t), 1);
+      mbar_init(bar(L::kBarPFull + t), 128);
+      mbar_init(bar(L::kBarODone + t), 1);
+    }
+    mbar_init(bar(L::kBarMmaDone), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(L::kCtlRegs));
+   if (warp == 0) {
+    // =========================== producer ===========================
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_q);
+      prefetch_tensormap(&p.tm_k);
+      prefetch_tensormap(&p.tm_v);
+      mbar_arrive_expect_tx(bar(L::kBarQFull), NQT * L::kQBytes);
+#pragma unroll
+      for (int t = 0; t < NQT; ++t)
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          tma_load_3d(sbase + t * L::kQBytes + c * kSubTile, &p.tm_q, c * 64, (qblock * NQT + t) * kTile, bh,
+                      bar(L::kBarQFull));
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nkv_max; ++j) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int ld = 2 * j + h;
+          const int s = ld % L::kStages;
+          if (!mbar_wait(bar(L::kBarKVEmpty + s), ((ld / L::kStages) & 1) ^ 1, ctl, kWhereProdEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sbase + L::kKVOff + s * L::kStageBytes;
+          if (h == 0) {
+            mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
+#pragma unroll
+            for (int c = 0; c < DQK / 64; ++c)
+              tma_load_3d(dst + c * kSubTile, &p.tm_k, c * 64, j * kTile, bh, bar(L::kBarKVFull + s));
+          } else {
+            mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kVBytes);
+#pragma unroll
+            for (int c = 0; c < DV / 64; ++c)
+              tma_load_3d(dst + c * kSubTile, &p.tm_v, c * 64, j * kTile, bh, bar(L::kBarKVFull + s));
+          }
+          issued = ld + 1;
+        }
+      }
+      // copies still in flight must land before the CTA can exit
+      mbar_wait_drain(bar(L::kBarQFull), 0, p.timeout_ns);
+      for (int ld = issued > L::kStages ? issued - L::kStages : 0; ld < issued; ++ld)
+        mbar_wait_drain(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    // =========================== MMA issuer =========================
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, false, true);
+      auto wait_load = [&](int ld) -> bool {
+        const bool r = mbar_wait(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1, ctl, kWhereMmaKV);
+        tc_fence_after();
+        return r;
+      };
+      auto issue_qk = [&](int t, int stage) {
+        const uint32_t qa = sbase + t * L::kQBytes;
+        const uint32_t kb = sbase + L::kKVOff + stage * L::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kSubTile + (kk % 4) * 32;
+          mma_ss(tmem + t * 256, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdescQK,
+                 kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int stage, bool acc) {
+        const uint32_t vb = sbase + L::kKVOff + stage * L::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_sw128(vb + kk * 2048, kSubTile, 1024),
+                 kIdescPV, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar(L::kBarQFull), 0, ctl, kWhereMmaQ);
+      if (ok && nkv_max > 0) {
+        ok = wait_load(0);
+        if (ok) {
+#pragma unroll
+          for (int t = 0; t < NQT; ++t)
+            if (nkv[t] > 0) {
+              issue_qk(t, 0);
+              tc_commit(bar(L::kBarSFull + t));
+            }
+          tc_commit(bar(L::kBarKVEmpty + 0));
+        }
+      }
+      for (int j = 0; ok && j < nkv_max; ++j) {
+        const int ldv = 2 * j + 1;
+        const int ldk = 2 * j + 2;
+        if (!(ok = wait_load(ldv))) break;
+        bool k_ready = false;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (ok && j < nkv[t]) {
+            ok = mbar_wait(bar(L::kBarPFull + t), j & 1, ctl, kWhereMmaP);
+            tc_fence_after();
+            if (ok) {
+              issue_pv(t, ldv % L::kStages, j > 0);
+              tc_commit(bar(L::kBarODone + t));
+            }
+          }
+          if (ok && j + 1 < nkv[t]) {
+            if (!k_ready) ok = k_ready = wait_load(ldk);
+            if (ok) {
+              issue_qk(t, ldk % L::kStages);
+              tc_commit(bar(L::kBarSFull + t));
+            }
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar(L::kBarKVEmpty + ldv % L::kStages));
+        if (k_ready) tc_commit(bar(L::kBarKVEmpty + ldk % L::kStages));
+      }
+      // every product issued above completes before tensor memory is freed
+      tc_commit(bar(L::kBarMmaDone));
+      mbar_wait_drain(bar(L::kBarMmaDone), 0, p.timeout_ns);
+    }
+    __syncwarp();
+   }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kSmRegs));
+    // ====================== softmax warpgroups =======================
+    const int t = (warp - 4) >> 2;
+    const int quad = warp & 3;  // this warp may touch tensor-memory lanes 32*quad .. 32*quad+31
+    const int qt = qblock * NQT + t;
+    const int q_row = qt * kTile + quad * 32 + lane;
+    const uint32_t tS = tmem + ((uint32_t)(quad * 32) << 16) + t * 256;
+    const uint32_t tO = tS + 128;
+    const int n = nkv[t];
+    const float c_log2 = p.scale_log2;
+    float m = -INFINITY;  // running (possibly stale) max, log2 units
+    float l = 0.f;        // running sum of 2^(s*c - m)
+    unsigned rescales = 0;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), j & 1, ctl, kWhereSmS));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+      tmem_ld32p(tS + 0, s + 0);
+      tmem_ld32p(tS + 32, s + 32);
+      tmem_ld32p(tS + 64, s + 64);
+      tmem_ld32p(tS + 96, s + 96);
+      const int kbase = j * kTile;
+      if ((CAUSAL && j == qt) || kbase + kTile > p.N) {
+        const int lim = CAUSAL ? min(q_row + 1, p.N) : p.N;  // keys < lim are visible
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (kbase + c >= lim) s[c] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_new = fmaxf(m, mx * c_log2);
+      const bool need = m_new > m + p.tau;
+      if (__any_sync(0xffffffffu, need)) {
+        // the warp moves every row to its current max (valid for all rows,
+        // since m_new >= m), so tensor-memory traffic stays warp-uniform
+        const float alpha = (m == -INFINITY) ? 0.f : ex2_mufu(m - m_new);
+        rescales += (j > 0 && need) ? 1u : 0u;
+        l *= alpha;
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), (j - 1) & 1, ctl, kWhereSmO));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < DV; c0 += 32) {
+            float o[32];
+            tmem_ld32(tO + c0, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tO + c0, o);
+          }
+        }
+        m = m_new;
+      }
+      const float m_use = (m == -INFINITY) ? 0.f : m;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float x0 = fmaf(s[c0 + i], c_log2, -m_use);
+          const float x1 = fmaf(s[c0 + i + 1], c_log2, -m_use);
+          const float e0 = (i < POLY) ? ex2_poly3(x0) : ex2_mufu(x0);
+          const float e1 = (i + 1 < POLY) ? ex2_poly3(x1) : ex2_mufu(x1);
+          ls[(i >> 1) & 3] += e0 + e1;
+          pk[i >> 1] = pack_bf16(e0, e1);
+        }
+        tmem_st16(tS + c0 / 2, pk);  // P (bf16 pairs) over the first 64 columns of S
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarPFull + t));
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), (n - 1) & 1, ctl, kWhereSmFinal));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const bool live = q_row < p.N;
+        uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                               ((size_t)bh * p.N + (live ? q_row : 0)) * DV);
+#pragma unroll
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+          float o[32];
+          tmem_ld32(tO + c0, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+          if (live) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        if (live) p.lse[(size_t)bh * p.N + q_row] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+    if (p.rescale_counter != nullptr) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) rescales += __shfl_xor_sync(0xffffffffu, rescales, off);
+      if (lane == 0 && rescales) atomicAdd(p.rescale_counter, (unsigned long long)rescales);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int DQK, int DV, int NQT, bool CAUSAL, int POLY>
+cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
+  using L = FwdLayout<DQK, DV, NQT>;
+  auto kernel = fwd_kernel<DQK, DV, NQT, CAUSAL, POLY>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // setmaxnreg.inc waits until the registers it asks for are free, so the
+  // split must add up to what the launch actually hands out
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != L::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  kernel<<<p.n_blocks, L::kThreads, L::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,161 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * What the library computes
+ * -------------------------
+ * Scaled-dot-product attention, exactly (up to floating-point rounding):
+ *
+ *     S = scale * Q K^T  (+ causal mask: key j hidden from query i when j > i)
+ *     O = softmax_rows(S) V,        LSE_i = log( sum_j exp(S_ij) )
+ *
+ * "Attention at Scale -- From FlashAttention to FlashAttention-4", section
+ * "The Problem", gives the definition (score matrix, softmax, product with V);
+ * the section "The Evolution" gives the tiled computation with a running
+ * row max and sum ("online softmax") that keeps the N x N matrix out of HBM.
+ * "FlashAttention 3 and 4: When the Bottleneck Moves", section 3.2, and the
+ * abstract of "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design
+ * for Asymmetric Hardware Scaling" give the forward's exponential split
+ * (hardware unit plus polynomial) and conditional rescaling; the same paper's
+ * Figure 2 and Table 3 give the backward's five matrix products, and its
+ * abstract and Figures 7-8 the atomic and deterministic dQ accumulation.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are dense, contiguous, row-major [B, H, N, d] arrays of bfloat16
+ *   in device memory (Q, K: d = d_qk; V, O, dO: d = d_v); LSE is FP32
+ *   [B, H, N].  N is the same for queries and keys.
+ * - Every device pointer must be 16-byte aligned.
+ * - Supported head dims (d_qk, d_v): (64, 64), (128, 128), (192, 128) for the
+ *   forward; (64, 64), (128, 128) for the backward.
+ * - B, H, N >= 1; B * H < 2^31; N < 2^24.
+ * - The caller owns every buffer, including the backward workspace.  The
+ *   library allocates no device memory; it keeps one device status word per
+ *   GPU.
+ * - Work is enqueued on ``stream`` (a cudaStream_t; NULL = legacy default
+ *   stream) and the call returns without synchronising.  Argument errors are
+ *   returned synchronously and nothing is launched.  Launch failures return
+ *   ATTN_ERR_CUDA.  Errors found by the kernels (a wait that ran past its time
+ *   limit) are recorded in the device status word; read them with
+ *   attn_get_device_status.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, size out of range, non-finite scale, bad flag */
+  ATTN_ERR_UNSUPPORTED = 2, /* head-dim pair not built */
+  ATTN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+  ATTN_ERR_WORKSPACE = 4,   /* backward workspace missing or smaller than attn_bwd_workspace_bytes */
+  ATTN_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed */
+  ATTN_ERR_TIMEOUT = 6,     /* device: a pipeline wait exceeded its time limit; outputs are invalid */
+  ATTN_ERR_BOUNDS = 7       /* device: an internal consistency check failed; outputs are invalid */
+} attn_status_t;
+
+/*
+ * Forward pass.
+ *   q [B,H,N,d_qk], k [B,H,N,d_qk], v [B,H,N,d_v]   bf16, read only
+ *   o [B,H,N,d_v]  bf16, written (softmax(S) V, normalised)
+ *   lse [B,H,N]    fp32, written: natural-log log-sum-exp of the scaled,
+ *                  unmasked scores of each query row (what the backward needs)
+ *   causal         0 or 1 (top-left aligned: query i sees keys 0..i)
+ *   scale          finite; usually 1/sqrt(d_qk)
+ * Returns ATTN_OK or an argument / launch error (see the enum).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d_qk,
+             int d_v, int causal, float scale, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for these sizes (0 for sizes the
+ * backward does not accept).  The workspace holds, per (b, h): the FP32 row
+ * terms D_i = dO_i . O_i and LSE_i * log2(e) (padded to a multiple of 128
+ * rows), the FP32 dQ accumulator, and (deterministic mode) one int32 ticket per
+ * 128-row query tile.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d_qk, int d_v, int deterministic);
+
+/*
+ * Backward pass: gradients of the forward with respect to q, k, v given dO.
+ *   q, k, v, o, dO  bf16 [B,H,N,d] as in attn_fwd (o is the forward's output)
+ *   lse             fp32 [B,H,N] from attn_fwd with the same arguments
+ *   dq, dk, dv      bf16 [B,H,N,d], overwritten (not accumulated)
+ *   deterministic   0: dQ partial sums are added in whatever order the tiles
+ *                      finish (results may differ in the last bits run to run);
+ *                   1: the additions into each dQ tile happen in a fixed
+ *                      order, so repeated calls give bit-identical dq, dk, dv.
+ *   workspace       device memory of at least attn_bwd_workspace_bytes bytes,
+ *                   16-byte aligned, owned by the caller, contents ignored on
+ *                   entry and clobbered.
+ * Returns ATTN_OK or an argument / launch error.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale,
+             int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises ``stream``, then returns and clears the device status word of
+ * the current device: ATTN_OK, or the first error a kernel recorded since the
+ * last call (ATTN_ERR_TIMEOUT, ATTN_ERR_BOUNDS).  If the stream itself
+ * reports a CUDA error, returns ATTN_ERR_CUDA.  ``where`` (may be NULL)
+ * receives the kernel's code for the wait or check that failed.
+ */
+int attn_get_device_status(cudaStream_t stream, int* where);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(int status);
+
+/*
+ * Accuracy probe of the exponential paths the forward uses.  Writes
+ * out[i] = 2^x[i] computed by ``method``: 0 = the hardware MUFU ex2.approx,
+ * 3 / 4 / 5 = the polynomial emulation of that degree (2^floor(x) * p(frac)).
+ * x and out are device FP32 arrays of n elements.  The cubic is the one the
+ * forward kernel uses.  "FlashAttention-4 ...", Table 2, reports the same
+ * measurement.
+ */
+int attn_exp2_probe(const float* x, float* out, int n, int method, cudaStream_t stream);
+
+/*
+ * Throughput probe: one launch over ``blocks`` blocks of 256 threads, each
+ * thread evaluating ``iters`` chained exponentials by ``method`` (as above).
+ * ``sink`` (device, >= blocks*256 floats) receives the results so the work is
+ * kept.  Time it with events on ``stream``.
+ */
+int attn_exp2_throughput(float* sink, int blocks, int iters, int method, cudaStream_t stream);
+
+/*
+ * Forward-pass rescale counter: when ``counter`` is a non-NULL device
+ * pointer, later attn_fwd calls on this device add to it the number of
+ * (row, key-tile) steps at which the running max rose by more than the
+ * threshold and the row was rescaled (first tiles not counted).  NULL turns
+ * counting off.  Returns ATTN_OK.
+ */
+int attn_set_rescale_counter(unsigned long long* counter);
+
+/*
+ * Threshold, in log2 units, for the conditional rescale of the running
+ * softmax state (default 8.0, i.e. a factor of 256; 0 rescales on every rise
+ * of the max).  Must be finite and in [0, 16].  Applies to later attn_fwd calls.
+ */
+int attn_set_rescale_threshold(float tau);
+
+/*
+ * Self-test of the kernels' bounded waits: launches one thread that waits on
+ * a pipeline barrier nothing will complete, with a limit of ``timeout_us``
+ * microseconds (1 .. 10^7).  The wait gives up, the kernel records
+ * ATTN_ERR_TIMEOUT in the device status word and returns, and the context
+ * stays usable; attn_get_device_status then reports it (where = 900).
+ */
+int attn_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -111,3 +111,61 @@ def attention_inputs(shape: AttentionShape, seed: int = 0, with_do: bool = True)
         pos += int(np.prod(shp))
         pos += pos % 2
     return out
+
+
+# ----------------------------------------------------------------------------
+# The same generator evaluated with torch tensors (on a GPU for large inputs).
+# Identical definition; int64 arithmetic wraps like uint64 and right shifts are
+# masked to be logical.  libm differences between devices can move an FP64
+# normal by an ulp, which after rounding to bfloat16 almost never shows; each
+# test therefore draws its inputs once and hands the same bits to both sides.
+def _as_i64(x: int) -> int:
+    x &= 0xFFFFFFFFFFFFFFFF
+    return x - (1 << 64) if x >= (1 << 63) else x
+
+
+def _lsr(t, k: int):
+    return (t >> k) & ((1 << (64 - k)) - 1)
+
+
+def normal_bf16_torch(seed: int, start: int, shape, device="cuda"):
+    """Like ``normal_bf16_bits`` but returns a torch.bfloat16 tensor on ``device``."""
+    import torch
+
+    if start % 2:
+        raise ValueError("start must be even")
+    count = int(np.prod(shape))
+    npairs = (count + 1) // 2
+    out = torch.empty(2 * npairs, dtype=torch.float64, device=device)
+    g, m1, m2, sd = _as_i64(0x9E3779B97F4A7C15), _as_i64(0xBF58476D1CE4E5B9), _as_i64(0x94D049BB133111EB), _as_i64(seed)
+    chunk = 1 << 24
+    for p0 in range(0, npairs, chunk):
+        p1 = min(npairs, p0 + chunk)
+        pairs = torch.arange(start // 2 + p0, start // 2 + p1, dtype=torch.int64, device=device)
+        u = []
+        for off in (0, 1):
+            z = (pairs * 2 + off + 1) * g + sd
+            z = (z ^ _lsr(z, 30)) * m1
+            z = (z ^ _lsr(z, 27)) * m2
+            z = z ^ _lsr(z, 31)
+            u.append(_lsr(z, 11).to(torch.float64) * (2.0 ** -53))
+        r = torch.sqrt(-2.0 * torch.log1p(-u[0]))
+        t = (2.0 * math.pi) * u[1]
+        out[2 * p0:2 * p1:2] = r * torch.cos(t)
+        out[2 * p0 + 1:2 * p1:2] = r * torch.sin(t)
+    return out[:count].to(torch.float32).to(torch.bfloat16).reshape(shape)
+
+
+def attention_inputs_torch(shape: AttentionShape, seed: int = 0, with_do: bool = True, device="cuda") -> dict:
+    """Q, K, V (and dO) as torch.bfloat16 tensors, same stream layout as ``attention_inputs``."""
+    B, H, N, dqk, dv = shape.B, shape.H, shape.N, shape.d_qk, shape.d_v
+    sizes = [("q", (B, H, N, dqk)), ("k", (B, H, N, dqk)), ("v", (B, H, N, dv))]
+    if with_do:
+        sizes.append(("do", (B, H, N, dv)))
+    out = {}
+    pos = 0
+    for name, shp in sizes:
+        out[name] = normal_bf16_torch(seed, pos, shp, device)
+        pos += int(np.prod(shp))
+        pos += pos % 2
+    return out

@@ -1,0 +1,213 @@
+"""GPU parity tests: the CUDA path (through the C ABI) against the FP64 oracle.
+
+Inputs are the seeded synthetic tensors of each workload (splitmix64 +
+Box-Muller, N(0,1), bfloat16, seed 0, drawn in the order Q, K, V, dO).  Small
+cases are compared element by element in full; the large configurations are
+compared on seeded samples of heads and query rows (forward; dQ rows) or on
+whole heads (dK, dV), each sampled row computed by the oracle against every
+key of its head.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import attention as ora
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_77_gb300 as A
+
+    A.get_lib()
+    yield A
+    G.check_status(A)
+
+
+def _full_fwd_check(A, B, H, N, dqk, dv, causal, seed=0):
+    t = G.inputs(B, H, N, dqk, dv, seed=seed, with_do=False)
+    o, lse = G.run_fwd(A, t, causal)
+    G.check_status(A)
+    q, k, v = (G.f64(t[n]) for n in ("q", "k", "v"))
+    o_ref, lse_ref = ora.forward(q, k, v, 1.0 / math.sqrt(dqk), causal)
+    return G.assert_fwd_close(G.f64(o), G.f64(lse), o_ref, lse_ref, f"B{B} H{H} N{N} d{dqk}/{dv} causal{causal}")
+
+
+# ------------------------------------------------ small, fully compared cases
+@pytest.mark.parametrize("causal", [0, 1])
+def test_pr1_forward_backward(A, causal):
+    """B=1, H=2, N=256, d=64, scale 1/8: forward and both backward modes, in full."""
+    B, H, N, d = 1, 2, 256, 64
+    t = G.inputs(B, H, N, d, d)
+    o, lse = G.run_fwd(A, t, causal)
+    q, k, v, do = (G.f64(t[n]) for n in ("q", "k", "v", "do"))
+    o_ref, lse_ref = ora.forward(q, k, v, 0.125, bool(causal))
+    G.assert_fwd_close(G.f64(o), G.f64(lse), o_ref, lse_ref)
+    dq_ref, dk_ref, dv_ref = ora.backward(q, k, v, do, 0.125, bool(causal))
+    for det in (0, 1):
+        dq, dk, dv = G.run_bwd(A, t, o, lse, causal, det)
+        G.check_status(A)
+        for name, got, ref in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+            e = G.rel_fro(G.f64(got), ref)
+            assert e <= G.GRAD_REL, (name, det, e)
+
+
+@pytest.mark.parametrize("dqk,dv", [(64, 64), (128, 128), (192, 128)])
+@pytest.mark.parametrize("N", [1, 17, 128, 129, 300, 640])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_forward_ragged_and_small(A, dqk, dv, N, causal):
+    _full_fwd_check(A, 1, 3, N, dqk, dv, bool(causal))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 100, 128, 257, 384])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("det", [0, 1])
+def test_backward_ragged_and_small(A, d, N, causal, det):
+    B, H = 1, 2
+    t = G.inputs(B, H, N, d, d, seed=3)
+    o, lse = G.run_fwd(A, t, causal)
+    dq, dk, dv = G.run_bwd(A, t, o, lse, causal, det)
+    G.check_status(A)
+    q, k, v, do = (G.f64(t[n]) for n in ("q", "k", "v", "do"))
+    refs = ora.backward(q, k, v, do, 1.0 / math.sqrt(d), bool(causal))
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        G.assert_grad_close(name, G.f64(got), ref)
+
+
+def test_multi_head_batch_layout(A):
+    """Several batches and heads, with a tail: every (b, h) lands in its own slot."""
+    _full_fwd_check(A, 3, 5, 200, 64, 64, True, seed=7)
+
+
+def test_special_inputs(A):
+    """V = ones gives O = ones; Q = 0 gives the (prefix) mean of V."""
+    torch = G.torch_mod()
+    t = G.inputs(1, 2, 300, 128, 128, seed=11, with_do=False)
+    t1 = dict(t, v=torch.ones_like(t["v"]))
+    o, _ = G.run_fwd(A, t1, 1)
+    # P enters the product as bf16 while the row sum keeps FP32, so O = 1 up to
+    # the bf16 rounding of P
+    assert float((o.float() - 1).abs().max()) <= 4e-3
+    t0 = dict(t, q=torch.zeros_like(t["q"]))
+    o, lse = G.run_fwd(A, t0, 1)
+    v = G.f64(t["v"])
+    prefix = np.cumsum(v, axis=2) / np.arange(1, 301)[None, None, :, None]
+    assert np.abs(G.f64(o) - prefix).max() <= G.O_MAX
+    np.testing.assert_allclose(G.f64(lse)[0, 0], np.log(np.arange(1, 301)), atol=G.LSE_MAX)
+
+
+def test_deterministic_backward_is_bit_identical(A):
+    torch = G.torch_mod()
+    t = G.inputs(2, 4, 1024, 128, 128, seed=5)
+    for causal in (0, 1):
+        o, lse = G.run_fwd(A, t, causal)
+        runs = [G.run_bwd(A, t, o, lse, causal, 1) for _ in range(3)]
+        G.check_status(A)
+        for r in runs[1:]:
+            for a, b in zip(runs[0], r):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_rescale_threshold_does_not_change_the_answer(A):
+    """tau = 0 (rescale on every rise) and tau = 8 agree within rounding."""
+    torch = G.torch_mod()
+    t = G.inputs(1, 4, 2048, 128, 128, seed=9, with_do=False)
+    t = dict(t, q=(t["q"].float() * 3).to(torch.bfloat16))  # sharper rows: the max moves more
+    counter = torch.zeros(1, dtype=torch.int64, device="cuda")
+    A.attn_set_rescale_counter(counter)
+    try:
+        A.attn_set_rescale_threshold(0.0)
+        o0, l0 = G.run_fwd(A, t, 0)
+        torch.cuda.synchronize()
+        n0 = int(counter.item())
+        counter.zero_()
+        A.attn_set_rescale_threshold(8.0)
+        o8, l8 = G.run_fwd(A, t, 0)
+        torch.cuda.synchronize()
+        n8 = int(counter.item())
+    finally:
+        A.attn_set_rescale_counter(None)
+        A.attn_set_rescale_threshold(8.0)
+    assert n8 < n0
+    # both meet the oracle; they differ only by bf16 rounding of P and O
+    q, k, v = (G.f64(t[n]) for n in ("q", "k", "v"))
+    o_ref, l_ref = ora.forward(q, k, v, 1.0 / math.sqrt(128), False)
+    G.assert_fwd_close(G.f64(o0), G.f64(l0), o_ref, l_ref, "tau=0")
+    G.assert_fwd_close(G.f64(o8), G.f64(l8), o_ref, l_ref, "tau=8")
+    assert float((l0 - l8).abs().max()) <= 1e-4
+
+
+def test_wait_timeout_is_reported_not_hung(A):
+    A.attn_selftest_wait_timeout(2000)
+    st, where = A.attn_get_device_status()
+    assert st == A.ATTN_ERR_TIMEOUT and where == 900
+    st, _ = A.attn_get_device_status()
+    assert st == 0
+    # the context still works afterwards
+    _full_fwd_check(A, 1, 1, 128, 64, 64, False)
+
+
+# --------------------------------------------- workload configs (sampled)
+def _sampled_fwd(A, B, H, N, dqk, dv, causal, n_heads, n_rows, seed_pick):
+    t = G.inputs(B, H, N, dqk, dv, with_do=False)
+    o, lse = G.run_fwd(A, t, causal)
+    G.check_status(A)
+    rng = np.random.Generator(np.random.PCG64(seed_pick))
+    all_heads = [(b, h) for b in range(B) for h in range(H)]
+    pick = [all_heads[i] for i in sorted(rng.choice(len(all_heads), size=min(n_heads, len(all_heads)), replace=False))]
+    rows = G.seeded_rows(N, n_rows, seed_pick + 1)
+    scale = 1.0 / math.sqrt(dqk)
+    worst = (0.0, 0.0, 0.0)
+    for (b, h) in pick:
+        q = G.f64(t["q"][b, h][rows])
+        k = G.f64(t["k"][b, h])
+        v = G.f64(t["v"][b, h])
+        o_ref, l_ref = ora.forward_head(q, k, v, scale, bool(causal), rows)
+        r = G.assert_fwd_close(G.f64(o[b, h][rows]), G.f64(lse[b, h][rows]), o_ref, l_ref, f"head {(b, h)}")
+        worst = tuple(max(x, y) for x, y in zip(worst, r))
+    return worst
+
+
+def test_config2_forward(A):
+    """B=2, H=16, N=2048, d=128, non-causal: all 32 heads x 256 rows, plus 2 full heads."""
+    _sampled_fwd(A, 2, 16, 2048, 128, 128, False, 32, 256, 20)
+    _sampled_fwd(A, 2, 16, 2048, 128, 128, False, 2, 2048, 21)
+
+
+@pytest.mark.parametrize("N", [1024, 2048, 4096, 8192, 16384])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_config3_forward_sweep(A, N, causal):
+    """d=128, H=16, B*N=16384: 4 seeded heads x 256 seeded rows."""
+    _sampled_fwd(A, 16384 // N, 16, N, 128, 128, bool(causal), 4, 256, 30 + N + causal)
+
+
+@pytest.mark.parametrize("N", [1024, 2048, 4096, 8192, 16384])
+def test_config4_forward_d192_causal(A, N):
+    """d_qk=192, d_v=128, H=16, B*N=16384, causal: 4 seeded heads x 256 seeded rows."""
+    _sampled_fwd(A, 16384 // N, 16, N, 192, 128, True, 4, 256, 40 + N)
+
+
+@pytest.mark.parametrize("N", [1024, 4096, 16384])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_config5_backward_sweep(A, N, causal):
+    """d=128, H=16, B*N=16384, both dQ modes: one seeded full head (dQ, dK, dV)."""
+    B, H, d = 16384 // N, 16, 128
+    t = G.inputs(B, H, N, d, d)
+    o, lse = G.run_fwd(A, t, causal)
+    rng = np.random.Generator(np.random.PCG64(50 + N + causal))
+    b, h = int(rng.integers(B)), int(rng.integers(H))
+    q, k, v, do = (G.f64(t[n][b, h]) for n in ("q", "k", "v", "do"))
+    refs = ora.backward_head(q, k, v, do, 1.0 / math.sqrt(d), bool(causal))
+    for det in (0, 1):
+        grads = G.run_bwd(A, t, o, lse, causal, det)
+        G.check_status(A)
+        for name, got, ref in zip(("dq", "dk", "dv"), grads, refs):
+            e = G.rel_fro(G.f64(got[b, h]), ref)
+            assert e <= G.GRAD_REL, (name, det, e)

@@ -39,3 +39,13 @@ def test_attention_inputs_order_and_shapes():
     t2 = synth.attention_inputs(s, seed=0)
     for name in t:
         np.testing.assert_array_equal(t[name], t2[name])
+
+
+def test_torch_generator_matches_numpy_on_cpu():
+    torch = __import__("pytest").importorskip("torch")
+    s = synth.AttentionShape(1, 2, 40, 8, 6)
+    a = synth.attention_inputs(s, seed=0)
+    b = synth.attention_inputs_torch(s, seed=0, device="cpu")
+    for name in a:
+        bits = b[name].view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(bits, a[name])
