@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = the whole hot path over one batch: forward (O, LSE) then backward
+(dQ, dK, dV) through the C ABI, on the workload B=1, H=16, N=16384,
+d_qk=d_v=128, non-causal, atomic dQ mode (the d=128, 16K-token point of the
+forward sweep and of the backward sweep).  Inputs are seeded synthetic BF16
+N(0,1) tensors already resident in HBM.
+
+Metric: BF16 attention TFLOPS (forward 4*B*H*N^2*d, halved for causal;
+backward 2.5x the forward) over the timed steps, and the dominant kernel's
+fraction of the measured dense BF16 peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the FP64 CPU oracle on the host cores (a bounded sample
+of the same workload per step).  Under torchrun every rank runs the same
+workload on its own GPU (independent replicas: no data exchange), timing is
+bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BF16 attention fwd+bwd TFLOPS on 1 GB300 (% of dense BF16 peak via roofline)"
+UNIT = "TFLOPS"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def workload(args):
+    return {"workload": f"attention fwd+bwd B={args.B} H={args.H} N={args.N} d={args.d} "
+                        f"{'causal' if args.causal else 'non-causal'} {'deterministic' if args.det else 'atomic'} dQ",
+            "B": args.B, "H": args.H, "N": args.N, "d_qk": args.d, "d_v": args.d, "causal": bool(args.causal),
+            "dq_mode": "deterministic" if args.det else "atomic", "scale": "1/sqrt(d)", "seed": 0,
+            "dtype_inputs": "bf16", "l2": "256 MiB write between timed steps (outside the timed events); "
+                                         "inputs 320 MiB > 129 MB L2"}
+
+
+def flops_fwd(a) -> float:
+    f = 4.0 * a.B * a.H * a.N * a.N * a.d
+    return f / 2 if a.causal else f
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of ``x`` across ranks (identity when world == 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.lines: list[str] = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd.insert(1, f"--id={gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_77_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, args):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    key = f"{kernel}:B{args.B}H{args.H}N{args.N}d{args.d}c{int(args.causal)}"
+    return rec.get("per_launch_bytes", {}).get(key)
+
+
+# ---------------------------------------------------------- CPU oracle
+def oracle_sample(args, rows: int = 1024):
+    """The oracle's forward and backward for ``rows`` query rows of head (0, 0)
+    against all N keys (non-causal rows are independent, so this is exactly
+    those rows' share of the workload).  Returns (seconds, flops, description)."""
+    import numpy as np
+
+    import synth
+    from oracle import attention as ora
+
+    # head (0, 0) of the workload's stream: Q, K, V, dO each start after the
+    # whole previous tensor (B*H*N*d draws)
+    per = args.B * args.H * args.N * args.d
+    draw = lambda start, n_rows: ora.bf16_to_f64(synth.normal_bf16_bits(0, start, (n_rows, args.d)))
+    q, k, v, do = draw(0, rows), draw(per, args.N), draw(2 * per, args.N), draw(3 * per, rows)
+    scale = 1.0 / math.sqrt(args.d)
+    t0 = time.perf_counter()
+    ora.forward_head(q, k, v, scale, bool(args.causal), np.arange(rows))
+    ora.backward_head(q, k, v, do, scale, bool(args.causal))
+    dt = time.perf_counter() - t0
+    fl = 3.5 * 4.0 * rows * args.N * args.d / (2 if args.causal else 1)
+    return dt, fl, f"head (0,0): {rows} of {args.N} query rows x {args.N} keys, forward + backward, FP64"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(args, min_seconds: float = 10.0) -> dict:
+    tot_t, tot_f, reps, desc = 0.0, 0.0, 0, ""
+    while tot_t < min_seconds and reps < 50:
+        dt, fl, desc = oracle_sample(args)
+        tot_t += dt
+        tot_f += fl
+        reps += 1
+    return {"value": tot_f / tot_t / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": f"{desc}; {reps} repetitions, {tot_t:.1f} s"}
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+
+    import exact_attention_77_gb300 as A
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    A.get_lib()
+    B, H, N, d = args.B, args.H, args.N, args.d
+    scale = 1.0 / math.sqrt(d)
+    t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, d, d), seed=0, device=dev)
+    q, k, v, do = t["q"], t["k"], t["v"], t["do"]
+    o = torch.empty_like(v)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nws = A.attn_bwd_workspace_bytes(B, H, N, d, d, args.det)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        A.attn_fwd(q, k, v, o, lse, B, H, N, d, d, args.causal, scale, stream)
+        A.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, d, args.causal, scale, args.det, ws, nws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, where = A.attn_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {A.status_string(st)} at {where}")
+
+    gpu_id = None
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    A.attn_profile_start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)  # evict the previous step's data from L2 (not timed)
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    prof = A.attn_profile_stop()
+    barrier(world)
+    clk = clocks.stop()
+    st, where = A.attn_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {A.status_string(st)} at {where}")
+    step_ms = sum(a.elapsed_time(b) for a, b in evs)
+    total_ms = max_over_ranks(step_ms, world, dev)
+
+    # end to end through the public API: pinned host buffers in, results out
+    hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+    ho, hlse, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, lse, dq, dk, dv))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_steps = max(2, args.steps // 2)
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+
+    f_fwd = flops_fwd(args)
+    f_step = 3.5 * f_fwd
+    value = world * f_step * args.steps / (total_ms / 1e3) / 1e12
+    peaks, peak_src = measured_peaks()
+    kernels = {
+        "attn_fwd_kernel": (prof["ms_fwd"], prof["launches_fwd"], f_fwd),
+        "attn_bwd_main_kernel": (prof["ms_bwd_main"], prof["launches_bwd_main"], 2.5 * f_fwd),
+    }
+    per_kernel = {}
+    for name, (ms, n, fl) in kernels.items():
+        avg = ms / max(n, 1)
+        ach = fl / (avg / 1e3) / 1e12 if avg > 0 else None
+        per_kernel[name] = {"launches": n, "avg_ms": avg, "achieved_tflops": ach}
+    dom = max(kernels, key=lambda n: kernels[n][0])
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    ach = per_kernel[dom]["achieved_tflops"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak if ach else None, "traffic": recorded_traffic(dom, args),
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a multi-kernel step)",
+                "frac_of_nominal_2250": ach / 2250.0 if ach else None}
+    fwd_ach = per_kernel["attn_fwd_kernel"]["achieved_tflops"]
+    roofline_fwd = {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": fwd_ach,
+                    "peak": peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]), "unit": "TFLOP/s",
+                    "frac": fwd_ach / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) if fwd_ach else None,
+                    "peak_source": f"{peak_src} bf16_tflops (burst)",
+                    "frac_of_nominal_2250": fwd_ach / 2250.0 if fwd_ach else None,
+                    "traffic": recorded_traffic("attn_fwd_kernel", args)}
+    launches = prof["launches_fwd"] + prof["launches_bwd_pre"] + prof["launches_bwd_main"] + prof["launches_bwd_convert"]
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16; splitmix64 + Box-Muller, seed 0)",
+        "config": dict(workload(args), parallelism=f"replicas{world}" if world > 1 else "single"),
+        "roofline": roofline, "roofline_fwd": roofline_fwd, "kernels": per_kernel,
+        "breakdown_tflops": {"forward": fwd_ach, "backward_main": per_kernel["attn_bwd_main_kernel"]["achieved_tflops"],
+                             "backward_incl_pre_convert": 2.5 * f_fwd / ((prof["ms_bwd_pre"] + prof["ms_bwd_main"] + prof["ms_bwd_convert"]) / max(prof["launches_bwd_main"], 1) / 1e3) / 1e12 if prof["launches_bwd_main"] else None},
+        "clocks": clk, "gpu_launches": launches,
+        "e2e": {"value": world * f_step / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args, world, rank):
+    """The oracle on the host cores: each step one bounded sample of the workload."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(args)
+    tot_t, tot_f, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        dt, fl, desc = oracle_sample(args)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1) bf16; splitmix64 + Box-Muller, seed 0)",
+           "config": dict(workload(args), parallelism="host cores"),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": desc},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--B", type=int, default=1)
+    ap.add_argument("--H", type=int, default=16)
+    ap.add_argument("--N", type=int, default=16384)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--causal", type=int, default=0)
+    ap.add_argument("--det", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    world, rank, local = dist_env()
+    if world != args.gpus and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

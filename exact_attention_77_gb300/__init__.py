@@ -39,7 +39,15 @@ _SIGS = {
     "attn_set_rescale_counter": (_I, [_P]),
     "attn_set_rescale_threshold": (_I, [_F]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
+    "attn_profile_start": (_I, []),
+    "attn_profile_stop": (_I, [_P]),
 }
+
+
+class attn_kernel_times_t(ctypes.Structure):
+    _fields_ = [("launches_fwd", _I), ("launches_bwd_pre", _I), ("launches_bwd_main", _I),
+                ("launches_bwd_convert", _I), ("ms_fwd", _F), ("ms_bwd_pre", _F), ("ms_bwd_main", _F),
+                ("ms_bwd_convert", _F)]
 
 
 class AttnError(RuntimeError):
@@ -148,3 +156,14 @@ def attn_set_rescale_threshold(tau: float):
 
 def attn_selftest_wait_timeout(timeout_us: int, stream=None):
     _check(get_lib().attn_selftest_wait_timeout(int(timeout_us), _stream(stream)))
+
+
+def attn_profile_start():
+    _check(get_lib().attn_profile_start())
+
+
+def attn_profile_stop() -> dict:
+    """Stop per-kernel timing; returns launch counts and summed milliseconds per kernel."""
+    t = attn_kernel_times_t()
+    _check(get_lib().attn_profile_stop(ctypes.byref(t)))
+    return {name: getattr(t, name) for name, _ in attn_kernel_times_t._fields_}

@@ -9,18 +9,11 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "attn.h"
 #include "kernels.h"
 #include "sm103.cuh"
-
-namespace attn {
-cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
-cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
-cudaError_t launch_fwd_d192(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
-cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s);
-cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s);
-}  // namespace attn
 
 __device__ attn::DeviceStatus g_attn_status;
 
@@ -45,6 +38,24 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+
+// Events recorded while profiling: kind 0 = forward, 1..3 = backward pieces.
+struct ProfileRecord {
+  int kind;
+  cudaEvent_t a, b;
+};
+bool g_profiling = false;
+std::vector<ProfileRecord> g_records;
+
+bool profiling() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_profiling;
+}
+
+void add_record(int kind, cudaEvent_t a, cudaEvent_t b) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_records.push_back({kind, a, b});
+}
 
 Settings settings() {
   std::lock_guard<std::mutex> lock(g_mu);
@@ -200,10 +211,19 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.n_blocks = BH * ((p.n_qtiles + nqt - 1) / nqt);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tau = cfg.tau;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  if (profiling()) {
+    if (cudaEventCreate(&ea) != cudaSuccess || cudaEventCreate(&eb) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaEventRecord(ea, stream);
+  }
   cudaError_t e;
   if (d_qk == 64) e = attn::launch_fwd_d64(p, causal != 0, nqt, cfg.fwd_poly, stream);
   else if (d_qk == 128) e = attn::launch_fwd_d128(p, causal != 0, nqt, cfg.fwd_poly, stream);
   else e = attn::launch_fwd_d192(p, causal != 0, nqt, cfg.fwd_poly, stream);
+  if (ea != nullptr) {
+    cudaEventRecord(eb, stream);
+    add_record(0, ea, eb);
+  }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -253,8 +273,15 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.BH = BH;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = d_qk == 64 ? attn::launch_bwd_d64(p, causal != 0, deterministic != 0, stream)
-                             : attn::launch_bwd_d128(p, causal != 0, deterministic != 0, stream);
+  attn::LaunchEvents evs{};
+  const bool prof = profiling();
+  if (prof)
+    for (auto& ev : evs.ev)
+      if (cudaEventCreate(&ev) != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaError_t e = d_qk == 64 ? attn::launch_bwd_d64(p, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr)
+                             : attn::launch_bwd_d128(p, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr);
+  if (prof)
+    for (int k = 0; k < 3; ++k) add_record(1 + k, evs.ev[k], evs.ev[k + 1]);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -284,6 +311,42 @@ int attn_exp2_throughput(float* sink, int blocks, int iters, int method, cudaStr
   if (!sink || blocks < 1 || iters < 1) return ATTN_ERR_INVALID_ARG;
   if (method != 0 && method != 3 && method != 4 && method != 5) return ATTN_ERR_INVALID_ARG;
   return attn::launch_exp2_throughput(sink, blocks, iters, method, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_profile_start(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_profiling = true;
+  return ATTN_OK;
+}
+
+int attn_profile_stop(attn_kernel_times_t* out) {
+  if (out == nullptr) return ATTN_ERR_INVALID_ARG;
+  std::vector<ProfileRecord> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_profiling) return ATTN_ERR_INVALID_ARG;
+    g_profiling = false;
+    recs.swap(g_records);
+  }
+  memset(out, 0, sizeof(*out));
+  int st = ATTN_OK;
+  // the backward's four events are shared by its three records: destroy each once
+  std::vector<cudaEvent_t> to_free;
+  for (const ProfileRecord& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+      st = ATTN_ERR_CUDA;
+    switch (r.kind) {
+      case 0: out->launches_fwd++; out->ms_fwd += ms; break;
+      case 1: out->launches_bwd_pre++; out->ms_bwd_pre += ms; break;
+      case 2: out->launches_bwd_main++; out->ms_bwd_main += ms; break;
+      default: out->launches_bwd_convert++; out->ms_bwd_convert += ms; break;
+    }
+    to_free.push_back(r.a);
+    if (r.kind == 0 || r.kind == 3) to_free.push_back(r.b);
+  }
+  for (cudaEvent_t e : to_free) cudaEventDestroy(e);
+  return st;
 }
 
 int attn_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream) {

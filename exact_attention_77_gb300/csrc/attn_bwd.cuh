@@ -475,8 +475,12 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
 }
 
 template <int D, bool CAUSAL, bool DET>
-cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream) {
+cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const LaunchEvents* evs) {
   using L = BwdLayout<D>;
+  auto mark = [&](int i) {
+    if (evs != nullptr && evs->ev[i] != nullptr) cudaEventRecord(evs->ev[i], stream);
+  };
+  mark(0);
   // preprocess: D, LSE2, zeroed accumulator / tickets
   {
     const long rows = (long)p.BH * p.Npad;
@@ -486,6 +490,7 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  mark(1);
   {
     auto kernel = bwd_kernel<D, CAUSAL, DET>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
@@ -494,11 +499,14 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  mark(2);
   {
     const long warps = ((long)p.BH * p.N + (32 / (D / 4)) - 1) / (32 / (D / 4));
     const long blocks = (warps * 32 + 255) / 256;
     dq_convert_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    mark(3);
+    return e;
   }
 }
 

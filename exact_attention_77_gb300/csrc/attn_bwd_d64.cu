@@ -3,9 +3,9 @@
 
 namespace attn {
 
-cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s) {
-  if (causal) return deterministic ? launch_bwd_instance<64, true, true>(p, s) : launch_bwd_instance<64, true, false>(p, s);
-  return deterministic ? launch_bwd_instance<64, false, true>(p, s) : launch_bwd_instance<64, false, false>(p, s);
+cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s, const LaunchEvents* ev) {
+  if (causal) return deterministic ? launch_bwd_instance<64, true, true>(p, s, ev) : launch_bwd_instance<64, true, false>(p, s, ev);
+  return deterministic ? launch_bwd_instance<64, false, true>(p, s, ev) : launch_bwd_instance<64, false, false>(p, s, ev);
 }
 
 }  // namespace attn

@@ -52,12 +52,21 @@ struct BwdParams {
   float scale_log2;
 };
 
-// Forward: one kernel launch.  variant selects tiles per CTA (1 or 2).
-cudaError_t launch_fwd(const FwdParams& p, int d_qk, int d_v, bool causal, int q_tiles_per_cta, cudaStream_t s);
-int fwd_blocks_per_unit(int q_tiles_per_cta);
+// Optional events recorded on the launch stream around each backward kernel:
+// ev[0] before the preprocess, ev[1] between preprocess and main, ev[2]
+// between main and dQ conversion, ev[3] after it.  Null entries are skipped.
+struct LaunchEvents {
+  cudaEvent_t ev[4];
+};
+
+// Forward (one kernel): per head-dim translation unit.
+cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
+cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
+cudaError_t launch_fwd_d192(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
 
 // Backward: preprocess, main, dQ conversion.
-cudaError_t launch_bwd(const BwdParams& p, int d_qk, int d_v, bool causal, bool deterministic, cudaStream_t s);
+cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s, const LaunchEvents* ev);
+cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s, const LaunchEvents* ev);
 
 // Probes of the exponential paths.
 cudaError_t launch_exp2_probe(const float* x, float* out, int n, int method, cudaStream_t s);

@@ -146,6 +146,25 @@ int attn_set_rescale_counter(unsigned long long* counter);
 int attn_set_rescale_threshold(float tau);
 
 /*
+ * Per-kernel timing for benchmarks.  Between attn_profile_start and
+ * attn_profile_stop, every attn_fwd / attn_bwd call on any stream also records
+ * CUDA events immediately before and after each of its kernel launches, on
+ * the launch stream.  attn_profile_stop synchronises those events and fills
+ * ``out`` with the launch counts and summed durations (milliseconds) per
+ * kernel: the forward kernel, and the backward's preprocess, main and dQ
+ * conversion kernels.  Profiling adds host work per call; leave it off
+ * otherwise.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG (null out / not started)
+ * or ATTN_ERR_CUDA.
+ */
+typedef struct {
+  int launches_fwd, launches_bwd_pre, launches_bwd_main, launches_bwd_convert;
+  float ms_fwd, ms_bwd_pre, ms_bwd_main, ms_bwd_convert;
+} attn_kernel_times_t;
+
+int attn_profile_start(void);
+int attn_profile_stop(attn_kernel_times_t* out);
+
+/*
  * Self-test of the kernels' bounded waits: launches one thread that waits on
  * a pipeline barrier nothing will complete, with a limit of ``timeout_us``
  * microseconds (1 .. 10^7).  The wait gives up, the kernel records

@@ -1,0 +1,52 @@
+"""CPU checks of bench.py's host logic: FLOP counting, the multi-rank timing
+reduction (two gloo ranks on CPU), and the oracle baseline sample."""
+import math
+import os
+import socket
+
+import pytest
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    out[rank] = bench.max_over_ranks(10.0 + rank * 5.0, world)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_rank_main, args=(2, _free_port(), out), nprocs=2, join=True)
+    assert dict(out) == {0: 15.0, 1: 15.0}
+
+
+def test_single_rank_reduction_is_identity():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_flop_convention():
+    a = type("A", (), dict(B=1, H=16, N=16384, d=128, causal=0))()
+    assert bench.flops_fwd(a) == 4 * 16 * 16384 ** 2 * 128
+    a.causal = 1
+    assert bench.flops_fwd(a) == 2 * 16 * 16384 ** 2 * 128
+
+
+def test_oracle_sample_runs_small():
+    a = type("A", (), dict(B=1, H=1, N=256, d=64, causal=0))()
+    dt, fl, desc = bench.oracle_sample(a, rows=64)
+    assert dt > 0 and fl == 3.5 * 4 * 64 * 256 * 64 and "64 of 256" in desc
