@@ -39,6 +39,7 @@ _SIGS = {
     "attn_set_rescale_counter": (_I, [_P]),
     "attn_set_rescale_threshold": (_I, [_F]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
+    "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_profile_start": (_I, []),
     "attn_profile_stop": (_I, [_P]),
 }
@@ -126,6 +127,20 @@ def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, causal, scale,
     st = get_lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N,
                       d_qk, d_v, int(causal), float(scale), int(deterministic), _ptr(workspace), int(workspace_bytes),
                       _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+ATTN_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, causal, scale, deterministic, stream=None,
+                     check=True) -> int:
+    """attn_bwd with the library's built-in scratch array as workspace (no allocation)."""
+    st = get_lib().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), B, H, N, d_qk, d_v, int(causal), float(scale), int(deterministic),
+                                    _stream(stream))
     if check:
         _check(st)
     return st

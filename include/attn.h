@@ -173,6 +173,35 @@ int attn_profile_stop(attn_kernel_times_t* out);
  */
 int attn_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
 
+/*
+ * Size of the device array attn_bwd_noalloc uses as its workspace: 32 MiB on
+ * every GPU that loads this library, held until the process exits.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * attn_bwd without a caller-provided workspace.  The pages describe no such
+ * call (it has no counterpart in the paper): it exists for callers that
+ * cannot allocate device memory -- code running in a host callback, or inside
+ * a runtime that hands out every device buffer itself and forbids
+ * allocations on its request path -- and so cannot supply attn_bwd's
+ * workspace.  The workspace is a static device array of
+ * ATTN_NOALLOC_SCRATCH_BYTES inside the library; nothing is allocated.
+ *   Arguments, layouts and results are those of attn_bwd without
+ *   ``workspace`` / ``workspace_bytes``.
+ *   Sizes whose attn_bwd_workspace_bytes exceeds ATTN_NOALLOC_SCRATCH_BYTES
+ *   return ATTN_ERR_WORKSPACE; other argument errors as attn_bwd.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   All calls on a device share the array: calls whose kernels can overlap on
+ *   the GPU (unordered streams) race and give wrong results.  Each call
+ *   clears what it needs at its start, so back-to-back calls are correct.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                     void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale,
+                     int deterministic, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
