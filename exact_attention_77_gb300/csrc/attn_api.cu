@@ -24,7 +24,7 @@ constexpr int kMaxDevices = 64;
 struct Settings {
   unsigned long long timeout_ns = 5ull * 1000 * 1000 * 1000;
   int fwd_tiles = 2;  // query tiles per forward CTA (d = 64 / 128)
-  int fwd_poly = 1;   // polynomial share of the exponentials on
+  int fwd_poly = 0;   // 1: a share of the exponentials on the FMA-pipe polynomial
   float tau = 8.0f;
   unsigned long long* rescale_counter = nullptr;
 };
@@ -149,7 +149,7 @@ WorkspaceLayout workspace_layout(int B, int H, int N, int d_qk, int deterministi
   w.d = round_up(w.lse2 + bh * npad * 4, 256);
   w.acc = round_up(w.d + bh * npad * 4, 256);
   w.tickets = round_up(w.acc + bh * npad * (size_t)d_qk * 4, 256);
-  w.total = round_up(w.tickets + (deterministic ? bh * tiles * 4 : 0), 256);
+  w.total = round_up(w.tickets + (deterministic ? bh * tiles * 2 * 4 : 0), 256);
   return w;
 }
 

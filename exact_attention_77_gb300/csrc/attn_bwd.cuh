@@ -23,14 +23,17 @@
 //                      dV  += P^T dO_i           (TS, P^T bf16 in tensor memory)
 //                      dK  += dS^T Q_i           (TS, dS^T bf16 in tensor memory)
 //                      dQ_i = dS K_j             (SS, dS bf16 in shared memory)
-//                    and adds dQ_i into the FP32 accumulator with bulk
-//                    reduce-add copies (atomic mode), or in ascending-j order
-//                    behind a per-(b, h, i) ticket (deterministic mode).
+//                    and adds dQ_i into the FP32 accumulator with 16-byte
+//                    vector reductions straight from registers (atomic
+//                    mode), or with the same reductions in ascending-j order
+//                    behind a per-(b, h, i, column half) ticket
+//                    (deterministic mode).
 //   dq_convert_kernel  dQ = scale * accumulator, as bf16 [B,H,N,d].
 //
 // Warp roles in bwd_kernel (320 threads): warp 0 producer (TMA), warp 1 MMA
-// issuer and tensor-memory owner, warps 2-5 the elementwise warpgroup (one
-// key row per thread), warps 6-9 the dQ warpgroup (one query row per thread).
+// issuer and tensor-memory owner, warps 2-5 and 6-9 two compute warpgroups
+// that split each tile's query columns for the elementwise step (one key row
+// per thread) and dQ's columns for its read-out (one query row per thread).
 #pragma once
 
 #include "kernels.h"
@@ -48,7 +51,7 @@ struct BwdLayout {
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;           // 2 stages
   static constexpr int kDOOff = kQOff + 2 * kTileBytes;      // 2 stages
-  static constexpr int kDSOff = kDOOff + 2 * kTileBytes;     // dS (bf16 128x128) / dQ staging
+  static constexpr int kDSOff = kDOOff + 2 * kTileBytes;     // dS (bf16 128x128), MN-major for the dQ product
   static constexpr int kDSBytes = kBTile * kBTile * 2;
   static constexpr int kVecOff = kDSOff + kDSBytes;          // 2 stages x (LSE2[128], D[128]) fp32
   static constexpr int kVecBytes = 2 * kBTile * 4;
@@ -64,7 +67,6 @@ struct BwdLayout {
     kBarDSFull,
     kBarDQFull,
     kBarDQFree,
-    kBarDSFree,
     kBarAccDone,
     kNumBars
   };
@@ -72,8 +74,8 @@ struct BwdLayout {
   static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   // tensor memory columns
-  static constexpr int kColS = 0;      // S^T fp32 [128 x 128]; P^T bf16 in its first 64 columns
-  static constexpr int kColDP = 128;   // dP^T fp32; dS^T bf16 in its first 64 columns
+  static constexpr int kColS = 0;      // S^T fp32 [128 x 128]; P^T bf16 packed in columns 0-31 and 64-95
+  static constexpr int kColDP = 128;   // dP^T fp32; dS^T bf16 packed the same way
   static constexpr int kColDV = 256;   // dV accumulator [128 x D]
   static constexpr int kColDK = 256 + D;
   static constexpr int kColDQ = D == 64 ? 384 : 0;  // d = 128 shares the S^T columns
@@ -133,9 +135,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdParams p) {
   for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += (size_t)gridDim.x * blockDim.x)
     acc4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (p.tickets != nullptr)
-    for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < (size_t)p.BH * p.n_tiles;
+    for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < (size_t)p.BH * p.n_tiles * 2;
          k += (size_t)gridDim.x * blockDim.x)
-      p.tickets[k] = 0;
+      p.tickets[k] = 0;  // two tickets (column halves) per (bh, query tile)
 }
 
 // ---------------------------------------------------------------- dQ out
@@ -178,12 +180,17 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
-  // work unit: key tile j of head bh; key-tile-major so that the CTAs a
-  // deterministic CTA waits for (smaller j, same head) were launched first,
-  // and (causal) the longest columns go first.
+  // work unit: key tile j of head bh.  Causal key tiles with small j are the
+  // longest (they see the most query tiles) and go first in either order.
   const int n = p.n_tiles;
-  const int j = blockIdx.x / p.BH;
-  const int bh = blockIdx.x - j * p.BH;
+  int j, bh;
+  if (DETERMINISTIC) {  // key-tile-major: a CTA waits only on CTAs launched before it
+    j = blockIdx.x / p.BH;
+    bh = blockIdx.x - j * p.BH;
+  } else {  // head-major: resident CTAs share one or two heads' dQ accumulators in L2
+    bh = blockIdx.x / n;
+    j = blockIdx.x - bh * n;
+  }
   const int i_lo = CAUSAL ? j : 0;  // query tiles i_lo .. n-1, visited from n-1 down
   const int n_it = n - i_lo;
   auto tile_of = [&](int it) { return n - 1 - it; };
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
   if (threadIdx.x == 0) {
     for (int b = 0; b < L::kNumBars; ++b) {
       uint32_t cnt = 1;
-      if (b == L::kBarDSFull || b == L::kBarDQFree) cnt = 128;
+      if (b == L::kBarDSFull || b == L::kBarDQFree) cnt = 256;
       mbar_init(bar(b), cnt);
     }
     *abort_flag = 0;
@@ -266,12 +273,14 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
                  kk > 0);
         }
       };
-      // C (+)= A[tmem, 128 x 128 bf16] B, B = [128 (K) x D] MN-major at b_base
+      // C (+)= A[tmem, 128 x 128 bf16] B, B = [128 (K) x D] MN-major at b_base.
+      // A's queries 64h..64h+63 sit packed in columns 64h..64h+31 (each
+      // compute warpgroup packs into the half of S^T / dP^T it read).
       auto mma_tmem_a = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kBTile / 16; ++kk)
-          mma_ts(tmem + d_col, tmem + a_col + kk * 8, sdesc_sw128(b_base + kk * 2048, kBSub, 1024), kIdAcc,
-                 (acc || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + d_col, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8,
+                 sdesc_sw128(b_base + kk * 2048, kBSub, 1024), kIdAcc, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar(L::kBarKV), 0, ctl, kBWhereMma);
       tc_fence_after();
@@ -309,79 +318,128 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
       mbar_wait_drain(bar(L::kBarAccDone), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // ======================= elementwise warpgroup ======================
+  } else {
+    // ================= two compute warpgroups (h = 0, 1) =================
+    // Warpgroup h owns query columns [64h, 64h + 64) of every tile for the
+    // elementwise step (keys on tensor-memory lanes) and dQ columns
+    // [h*D/2, (h+1)*D/2) for the read-out (queries on lanes).
+    const int h = (warp - 2) >> 2;
     const int quad = warp & 3;
-    const int krow = quad * 32 + lane;  // key row within the tile (tensor-memory lane)
-    const int k_glob = j * kBTile + krow;
+    const int lrow = quad * 32 + lane;      // tensor-memory lane: key row / query row
+    const int tid = threadIdx.x - 64 - 128 * h;  // 0..127 within the warpgroup
+    const int k_glob = j * kBTile + lrow;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + L::kColS;
     const uint32_t tDP = tmem + lane_base + L::kColDP;
+    const uint32_t tDQ = tmem + lane_base + L::kColDQ + h * (D / 2);
+    uint8_t* ds_half = smem + L::kDSOff + h * kBSub;  // dS query chunk h (queries 64h .. 64h+63)
     const float c_log2 = p.scale_log2;
+    const bool key_dead = k_glob >= p.N;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
       const int i = tile_of(it);
-      // the stage's LSE2 / D vectors arrive with Q_i on the same barrier
+      // LSE2 / D vectors arrive with Q_i on the stage's barrier
       ok = mbar_wait(bar(L::kBarQFull + s), (it >> 1) & 1, ctl, kBWhereEw + 3);
       ok = ok && mbar_wait(bar(L::kBarSFull), it & 1, ctl, kBWhereEw);
       ok = ok && mbar_wait(bar(L::kBarDPFull), it & 1, ctl, kBWhereEw + 1);
-      // the dS buffer doubles as dQ staging: wait until its bulk reads are done
-      ok = ok && (it == 0 || mbar_wait(bar(L::kBarDSFree), (it - 1) & 1, ctl, kBWhereEw + 2));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(smem + L::kVecOff + s * L::kVecBytes);
       const bool diag = CAUSAL && i == j;
-      const bool key_dead = k_glob >= p.N;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kBTile; c0 += 32) {
+#pragma unroll
+      for (int c0 = 64 * h; c0 < 64 * h + 64; c0 += 32) {
         float sv[32], dp[32];
         tmem_ld32(tS + c0, sv);
         tmem_ld32(tDP + c0, dp);
         uint32_t pk[16], dk[16];
-        float dsv[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
+        for (int q = 0; q < 32; q += 2) {
           const int qi = c0 + q;
-          float pv = ex2_mufu(fmaf(sv[q], c_log2, -vec[qi]));
-          if (key_dead || (diag && (i * kBTile + qi) < k_glob)) pv = 0.f;
-          const float ds = pv * (dp[q] - vec[kBTile + qi]);
-          dsv[q] = ds;
-          sv[q] = pv;
+          const float2 x = __ffma2_rn(make_float2(sv[q], sv[q + 1]), make_float2(c_log2, c_log2),
+                                      make_float2(-vec[qi], -vec[qi + 1]));
+          float p0 = ex2_mufu(x.x), p1 = ex2_mufu(x.y);
+          if (key_dead || (diag && (i * kBTile + qi) < k_glob)) p0 = 0.f;
+          if (key_dead || (diag && (i * kBTile + qi + 1) < k_glob)) p1 = 0.f;
+          const float2 ds = __fmul2_rn(make_float2(p0, p1),
+                                       __fadd2_rn(make_float2(dp[q], dp[q + 1]),
+                                                  make_float2(-vec[kBTile + qi], -vec[kBTile + qi + 1])));
+          pk[q >> 1] = pack_bf16(p0, p1);
+          dk[q >> 1] = pack_bf16(ds.x, ds.y);
         }
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          pk[q] = pack_bf16(sv[2 * q], sv[2 * q + 1]);
-          dk[q] = pack_bf16(dsv[2 * q], dsv[2 * q + 1]);
-        }
-        tmem_st16(tS + c0 / 2, pk);
-        tmem_st16(tDP + c0 / 2, dk);
+        // packed bf16 pairs stay inside this warpgroup's half of the columns
+        const int pcol = 64 * h + (c0 % 64) / 2;
+        tmem_st16(tS + pcol, pk);
+        tmem_st16(tDP + pcol, dk);
         // dS (queries x keys) into shared memory, MN-major with the 128-byte
-        // swizzle: query chunk (c0/64) at 16 KB, key row krow at
-        // (krow/8)*1024 + (krow%8)*128, 16-byte unit (q%64)/8 xor (krow%8).
-        uint8_t* ds_base = smem + L::kDSOff + (c0 / 64) * kBSub + (krow >> 3) * 1024 + (krow & 7) * 128;
+        // swizzle: query chunk h at 16 KB, key row lrow at
+        // (lrow/8)*1024 + (lrow%8)*128, 16-byte unit (q%64)/8 xor (lrow%8).
+        uint8_t* ds_row = ds_half + (lrow >> 3) * 1024 + (lrow & 7) * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int unit = ((c0 % 64) / 8 + u) ^ (krow & 7);
-          *reinterpret_cast<uint4*>(ds_base + unit * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+          const int unit = ((c0 % 64) / 8 + u) ^ (lrow & 7);
+          *reinterpret_cast<uint4*>(ds_row + unit * 16) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
       }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(L::kBarDSFull));
+
+      // ---- dQ_i read-out: this warpgroup's D/2 columns, then FP32 reductions
+      // into the accumulator (the dQ product has also finished reading dS, so
+      // the next tile's dS may be written after this point)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
+      if (!ok) break;
+      tc_fence_after();
+      float dq[D / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < D / 2; c0 += 32) tmem_ld32p(tDQ + c0, dq + c0);
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDQFree));  // tensor-memory dQ columns may be overwritten
+      // accumulator layout per (bh, i): [D/4 column groups][128 rows][4]; this
+      // warpgroup's groups are h*D/8 .. (h+1)*D/8 - 1.  A warp's 16-byte
+      // reductions to one group cover 512 contiguous bytes.
+      float4* gdst = reinterpret_cast<float4*>(p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile)) +
+                     (size_t)h * (D / 8) * kBTile + lrow;
+      int* ticket = DETERMINISTIC ? p.tickets + ((size_t)bh * p.n_tiles + i) * 2 + h : nullptr;
+      if (DETERMINISTIC) {
+        if (tid == 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(ticket) != j) {  // tile i takes key tiles in ascending j
+            if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
+              if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
+              *ctl.abort = 1;
+              break;
+            }
+          }
+        }
+        named_bar_sync(1 + h, 128);  // every thread's additions come after the acquire
+      }
+      if (!*ctl.abort) {
+#pragma unroll
+        for (int g = 0; g < D / 8; ++g)
+          atomicAdd(gdst + (size_t)g * kBTile, make_float4(dq[4 * g], dq[4 * g + 1], dq[4 * g + 2], dq[4 * g + 3]));
+      }
+      if (DETERMINISTIC) {
+        __threadfence();
+        named_bar_sync(1 + h, 128);
+        if (tid == 0 && !*ctl.abort) red_release_gpu_add(ticket, 1);
+      }
     }
-    // epilogue: dV, dK rows of this key tile
+    // epilogue: dV and dK rows of this key tile; warpgroup h writes columns
+    // [h*D/2, (h+1)*D/2)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, ctl, kBWhereFin));
     if (ok) {
       tc_fence_after();
-      const bool live = k_glob < p.N;
+      const bool live = !key_dead;
       const size_t row = (size_t)bh * p.N + (live ? k_glob : 0);
       uint4* dvrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dv) + row * D);
       uint4* dkrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dk) + row * D);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
         float a[32], b[32];
         tmem_ld32(tmem + lane_base + L::kColDV + c0, a);
         tmem_ld32(tmem + lane_base + L::kColDK + c0, b);
@@ -400,70 +458,6 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
         }
       }
     }
-  } else {
-    // =========================== dQ warpgroup ===========================
-    const int quad = warp & 3;
-    const int qrow = quad * 32 + lane;  // query row within the tile (tensor-memory lane)
-    const int tid = threadIdx.x - 192;  // 0..127 within the warpgroup
-    const uint32_t tDQ = tmem + ((uint32_t)(quad * 32) << 16) + L::kColDQ;
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int i = tile_of(it);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
-      if (!ok) break;
-      tc_fence_after();
-      float dq[D];
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32p(tDQ + c0, dq + c0);
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarDQFree));  // tensor-memory dQ columns may be overwritten
-      // stage through the dS buffer (its last reader, the dQ product, is done)
-      // in [column group][row][4] order, 16 KB (32 columns) per bulk reduction
-      float* gdst = p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile);
-      if (DETERMINISTIC && tid == 0) {
-        const int* tk = p.tickets + (size_t)bh * p.n_tiles + i;
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(tk) != j) {  // tile i takes key tiles in ascending j
-          if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
-            if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
-            *ctl.abort = 1;
-            break;
-          }
-        }
-        fence_proxy_async_global();
-      }
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        const int buf = c & 1;
-        if (c >= 2) {
-          if (tid == 0) bulk_wait_read<1>();
-          named_bar_sync(1, 128);
-        }
-        float* st = reinterpret_cast<float*>(smem + L::kDSOff + buf * 16384);
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<float4*>(st + (g * 128 + qrow) * 4) =
-              make_float4(dq[c * 32 + 4 * g], dq[c * 32 + 4 * g + 1], dq[c * 32 + 4 * g + 2], dq[c * 32 + 4 * g + 3]);
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (tid == 0 && !*ctl.abort) {
-          bulk_reduce_add_f32(gdst + (size_t)c * 32 * kBTile, smem_u32(st), 16384);
-          bulk_commit();
-        }
-      }
-      if (tid == 0) {
-        if (DETERMINISTIC) {
-          bulk_wait_all<0>();
-          fence_proxy_async_global();
-          if (!*ctl.abort) red_release_gpu_add(p.tickets + (size_t)bh * p.n_tiles + i, 1);
-        } else {
-          bulk_wait_read<0>();
-        }
-        mbar_arrive(bar(L::kBarDSFree));  // the dS buffer may be rewritten
-      }
-      __syncwarp();
-    }
-    if (tid == 0) bulk_wait_all<0>();
   }
 
   tc_fence_before();

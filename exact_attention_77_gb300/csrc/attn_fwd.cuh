@@ -62,8 +62,8 @@ struct FwdLayout {
   // the control warpgroup drops to kCtlRegs and each softmax warpgroup rises
   // to kSmRegs.  kCtlRegs * 128 + kSmRegs * 128 * NQT == kLaunchRegs * kThreads.
   static constexpr int kLaunchRegs = NQT == 1 ? 128 : 168;
-  static constexpr int kCtlRegs = NQT == 1 ? 40 : 56;
-  static constexpr int kSmRegs = NQT == 1 ? 216 : 224;
+  static constexpr int kCtlRegs = NQT == 1 ? 48 : 88;
+  static constexpr int kSmRegs = NQT == 1 ? 208 : 208;
   static_assert(kCtlRegs * 128 + kSmRegs * 128 * NQT == kLaunchRegs * kThreads, "register split");
   static constexpr int kKVOff = kQRegion;
   static constexpr int kBarOff = kKVOff + kStages * kStageBytes;
@@ -209,21 +209,20 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
         return r;
       };
       auto issue_qk = [&](int t, int stage) {
-        const uint32_t qa = sbase + t * L::kQBytes;
-        const uint32_t kb = sbase + L::kKVOff + stage * L::kStageBytes;
+        const uint64_t da = sdesc_sw128(sbase + t * L::kQBytes, 16, 1024);
+        const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk / 4) * kSubTile + (kk % 4) * 32;
-          mma_ss(tmem + t * 256, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdescQK,
-                 kk > 0);
+          mma_ss(tmem + t * 256, sdesc_advance(da, off), sdesc_advance(db, off), kIdescQK, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int stage, bool acc) {
-        const uint32_t vb = sbase + L::kKVOff + stage * L::kStageBytes;
+        const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, kSubTile, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_sw128(vb + kk * 2048, kSubTile, 1024),
-                 kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * 2048), kIdescPV,
+                 (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar(L::kBarQFull), 0, ctl, kWhereMmaQ);
       if (ok && nkv_max > 0) {
@@ -291,10 +290,14 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       if (!ok) break;
       tc_fence_after();
       float s[128];
-      tmem_ld32p(tS + 0, s + 0);
-      tmem_ld32p(tS + 32, s + 32);
-      tmem_ld32p(tS + 64, s + 64);
-      tmem_ld32p(tS + 96, s + 96);
+      if constexpr (NQT == 1) {  // 128 registers per thread: load in 32-column pieces
+        tmem_ld32p(tS + 0, s + 0);
+        tmem_ld32p(tS + 32, s + 32);
+        tmem_ld32p(tS + 64, s + 64);
+        tmem_ld32p(tS + 96, s + 96);
+      } else {
+        tmem_ld128(tS, s);
+      }
       const int kbase = j * kTile;
       if ((CAUSAL && j == qt) || kbase + kTile > p.N) {
         const int lim = CAUSAL ? min(q_row + 1, p.N) : p.N;  // keys < lim are visible
@@ -304,9 +307,9 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       }
       float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      for (int c = 16; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m, mx * c_log2);
@@ -333,22 +336,25 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
         m = m_new;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // x = s * scale * log2(e) - m on pairs (packed FP32 FMA), then 2^x
+      const float2 c2 = make_float2(c_log2, c_log2);
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float x0 = fmaf(s[c0 + i], c_log2, -m_use);
-          const float x1 = fmaf(s[c0 + i + 1], c_log2, -m_use);
-          const float e0 = (i < POLY) ? ex2_poly3(x0) : ex2_mufu(x0);
-          const float e1 = (i + 1 < POLY) ? ex2_poly3(x1) : ex2_mufu(x1);
-          ls[(i >> 1) & 3] += e0 + e1;
+          const float2 x = __ffma2_rn(make_float2(s[c0 + i], s[c0 + i + 1]), c2, nm2);
+          const float e0 = (i < POLY) ? ex2_poly3(x.x) : ex2_mufu(x.x);
+          const float e1 = (i + 1 < POLY) ? ex2_poly3(x.y) : ex2_mufu(x.y);
+          ls[(i >> 1) & 3] = __fadd2_rn(ls[(i >> 1) & 3], make_float2(e0, e1));
           pk[i >> 1] = pack_bf16(e0, e1);
         }
         tmem_st16(tS + c0 / 2, pk);  // P (bf16 pairs) over the first 64 columns of S
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      const float2 lsum = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+      l += lsum.x + lsum.y;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + t));
