@@ -149,7 +149,7 @@ WorkspaceLayout workspace_layout(int B, int H, int N, int d_qk, int deterministi
   w.d = round_up(w.lse2 + bh * npad * 4, 256);
   w.acc = round_up(w.d + bh * npad * 4, 256);
   w.tickets = round_up(w.acc + bh * npad * (size_t)d_qk * 4, 256);
-  w.total = round_up(w.tickets + (deterministic ? bh * tiles * 2 * 4 : 0), 256);
+  w.total = round_up(w.tickets + (deterministic ? bh * tiles * 4 : 0), 256);
   return w;
 }
 

@@ -11,8 +11,9 @@
 // and the deterministic accumulation of dQ.
 //
 // Kernels:
-//   bwd_pre_kernel   D_i = rowsum(dO o O) and LSE_i * log2(e) into the
-//                    workspace (padding rows: D = 0, LSE2 = +inf so P = 0);
+//   bwd_pre_kernel   -D_i = -rowsum(dO o O) and -LSE_i * log2(e) into the
+//                    workspace (negated so the main kernel adds them; padding
+//                    rows: 0 and -inf, so P = 0 there);
 //                    zeroes the FP32 dQ accumulator and the tickets.
 //   bwd_kernel       one CTA per (b, h, 128-key tile j), K_j and V_j resident;
 //                    for each query tile i it runs, with keys on the tensor-
@@ -26,15 +27,19 @@
 //                    and adds dQ_i into the FP32 accumulator with 16-byte
 //                    vector reductions straight from registers (atomic
 //                    mode), or with the same reductions in ascending-j order
-//                    behind a per-(b, h, i, column half) ticket
+//                    behind a per-(b, h, i) ticket
 //                    (deterministic mode).
 //   dq_convert_kernel  dQ = scale * accumulator, as bf16 [B,H,N,d].
 //
-// Warp roles in bwd_kernel (320 threads): warp 0 producer (TMA), warp 1 MMA
-// issuer and tensor-memory owner, warps 2-5 and 6-9 two compute warpgroups
+// Warp roles in bwd_kernel (512 threads): warp 0 producer (TMA), warp 1 MMA
+// issuer and tensor-memory owner, warps 4-7 and 8-11 two compute warpgroups
 // that split each tile's query columns for the elementwise step (one key row
-// per thread) and dQ's columns for its read-out (one query row per thread).
+// per thread), warps 12-15 the dQ warpgroup (one query row per thread) that
+// reads dQ out of tensor memory and issues its reductions off the critical
+// path.
 #pragma once
+
+#include <type_traits>
 
 #include "kernels.h"
 #include "sm103.cuh"
@@ -79,7 +84,15 @@ struct BwdLayout {
   static constexpr int kColDV = 256;   // dV accumulator [128 x D]
   static constexpr int kColDK = 256 + D;
   static constexpr int kColDQ = D == 64 ? 384 : 0;  // d = 128 shares the S^T columns
-  static constexpr int kThreads = 320;
+  // 16 warps in four warpgroups: control (producer, MMA issuer), two compute
+  // warpgroups, one dQ warpgroup.  setmaxnreg split of the 128 registers a
+  // thread gets at launch: 72 * 128 + 144 * 256 + 144 * 128 <= 128 * 512.
+  static constexpr int kThreads = 512;
+  static constexpr int kLaunchRegs = 128;
+  static constexpr int kCtlRegs = 72;
+  static constexpr int kComputeRegs = 144;
+  static constexpr int kDqRegs = 144;
+  static_assert(kCtlRegs * 128 + kComputeRegs * 256 + kDqRegs * 128 <= kLaunchRegs * kThreads, "register split");
 };
 
 enum : int {
@@ -126,8 +139,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdParams p) {
 #pragma unroll
   for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, kLanes);
   if (in_range && sub == 0) {
-    p.row_d[row] = acc;
-    p.row_lse2[row] = i < p.N ? p.lse[(size_t)bh * p.N + i] * 1.4426950408889634f : INFINITY;
+    p.row_d[row] = -acc;
+    p.row_lse2[row] = i < p.N ? -p.lse[(size_t)bh * p.N + i] * 1.4426950408889634f : -INFINITY;
   }
   // zero the dQ accumulator and the tickets (grid-stride, 16-byte stores)
   const size_t n4 = (size_t)p.BH * p.Npad * D / 4;
@@ -135,9 +148,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdParams p) {
   for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += (size_t)gridDim.x * blockDim.x)
     acc4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (p.tickets != nullptr)
-    for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < (size_t)p.BH * p.n_tiles * 2;
+    for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < (size_t)p.BH * p.n_tiles;
          k += (size_t)gridDim.x * blockDim.x)
-      p.tickets[k] = 0;  // two tickets (column halves) per (bh, query tile)
+      p.tickets[k] = 0;  // one ticket per (bh, query tile)
 }
 
 // ---------------------------------------------------------------- dQ out
@@ -165,7 +178,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(BwdParams p) {
 
 // ---------------------------------------------------------------- main
 template <int D, bool CAUSAL, bool DETERMINISTIC>
-__global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -198,7 +211,8 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
   if (threadIdx.x == 0) {
     for (int b = 0; b < L::kNumBars; ++b) {
       uint32_t cnt = 1;
-      if (b == L::kBarDSFull || b == L::kBarDQFree) cnt = 256;
+      if (b == L::kBarDSFull) cnt = 256;  // both compute warpgroups
+      if (b == L::kBarDQFree) cnt = 128;  // the dQ warpgroup
       mbar_init(bar(b), cnt);
     }
     *abort_flag = 0;
@@ -213,7 +227,9 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp < 4) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(L::kCtlRegs));
+   if (warp == 0) {
     // ============================ producer ============================
     if (lane == 0) {
       prefetch_tensormap(&p.tm_q);
@@ -241,6 +257,7 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
         bulk_load(sbase + L::kVecOff + s * L::kVecBytes, p.row_lse2 + vrow, kBTile * 4, bar(L::kBarQFull + s));
         bulk_load(sbase + L::kVecOff + s * L::kVecBytes + kBTile * 4, p.row_d + vrow, kBTile * 4,
                   bar(L::kBarQFull + s));
+        ATTN_TRACE_AT(blockIdx.x, it, 13);
         if (!mbar_wait(bar(L::kBarDOEmpty + s), ph, ctl, kBWhereProd + 1)) {
           issued = it + 1;
           break;
@@ -250,6 +267,7 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sbase + L::kDOOff + s * L::kTileBytes + c * kBSub, &p.tm_do, c * 64, i * kBTile, bh,
                       bar(L::kBarDOFull + s));
+        ATTN_TRACE_AT(blockIdx.x, it, 14);
         issued = it + 1;
       }
       mbar_wait_drain(bar(L::kBarKV), 0, p.timeout_ns);
@@ -290,16 +308,22 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
         const uint32_t qs = sbase + L::kQOff + s * L::kTileBytes;
         const uint32_t dos = sbase + L::kDOOff + s * L::kTileBytes;
         if (!(ok = mbar_wait(bar(L::kBarQFull + s), ph, ctl, kBWhereMma + 1))) break;
+        ATTN_TRACE_AT(blockIdx.x, it, 0);
         if (L::kColDQ == L::kColS && it > 0)  // S^T columns still hold dQ of the previous tile
           if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 2))) break;
+        ATTN_TRACE_AT(blockIdx.x, it, 1);
         tc_fence_after();
         mma_kmajor(L::kColS, sbase + L::kKOff, qs);
         tc_commit(bar(L::kBarSFull));
+        ATTN_TRACE_AT(blockIdx.x, it, 10);
         if (!(ok = mbar_wait(bar(L::kBarDOFull + s), ph, ctl, kBWhereMma + 3))) break;
+        ATTN_TRACE_AT(blockIdx.x, it, 2);
         tc_fence_after();
         mma_kmajor(L::kColDP, sbase + L::kVOff, dos);
         tc_commit(bar(L::kBarDPFull));
+        ATTN_TRACE_AT(blockIdx.x, it, 12);
         if (!(ok = mbar_wait(bar(L::kBarDSFull), it & 1, ctl, kBWhereMma + 4))) break;
+        ATTN_TRACE_AT(blockIdx.x, it, 3);
         tc_fence_after();
         mma_tmem_a(L::kColDV, L::kColS, dos, it > 0);
         mma_tmem_a(L::kColDK, L::kColDP, qs, it > 0);
@@ -313,25 +337,29 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
           mma_ss(tmem + L::kColDQ, sdesc_sw128(sbase + L::kDSOff + kk * 2048, kBSub, 1024),
                  sdesc_sw128(sbase + L::kKOff + kk * 2048, kBSub, 1024), kIdDq, kk > 0);
         tc_commit(bar(L::kBarDQFull));
+        ATTN_TRACE_AT(blockIdx.x, it, 4);
       }
       tc_commit(bar(L::kBarAccDone));
       mbar_wait_drain(bar(L::kBarAccDone), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else {
+   }
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kComputeRegs));
     // ================= two compute warpgroups (h = 0, 1) =================
     // Warpgroup h owns query columns [64h, 64h + 64) of every tile for the
-    // elementwise step (keys on tensor-memory lanes) and dQ columns
-    // [h*D/2, (h+1)*D/2) for the read-out (queries on lanes).
-    const int h = (warp - 2) >> 2;
+    // elementwise step (keys on tensor-memory lanes) and columns
+    // [h*D/2, (h+1)*D/2) of the dV / dK epilogue.  The next tile's dS is only
+    // written after its S^T product completed, and that product was issued
+    // after this tile's dQ product (which reads dS), so the buffer is free.
+    const int h = (warp - 4) >> 2;
     const int quad = warp & 3;
-    const int lrow = quad * 32 + lane;      // tensor-memory lane: key row / query row
-    const int tid = threadIdx.x - 64 - 128 * h;  // 0..127 within the warpgroup
+    const int lrow = quad * 32 + lane;      // tensor-memory lane: key row
+    const int tid = threadIdx.x - 128 - 128 * h;  // 0..127 within the warpgroup
     const int k_glob = j * kBTile + lrow;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + L::kColS;
     const uint32_t tDP = tmem + lane_base + L::kColDP;
-    const uint32_t tDQ = tmem + lane_base + L::kColDQ + h * (D / 2);
     uint8_t* ds_half = smem + L::kDSOff + h * kBSub;  // dS query chunk h (queries 64h .. 64h+63)
     const float c_log2 = p.scale_log2;
     const bool key_dead = k_glob >= p.N;
@@ -345,89 +373,64 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
       ok = ok && mbar_wait(bar(L::kBarDPFull), it & 1, ctl, kBWhereEw + 1);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 5 + h);
       tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(smem + L::kVecOff + s * L::kVecBytes);
       const bool diag = CAUSAL && i == j;
+      // the mask only bites on the diagonal tile and on a ragged last key tile
+      const bool mask_tile = diag || (j * kBTile + kBTile > p.N);
+      auto half_tile = [&](auto masked) {
 #pragma unroll
-      for (int c0 = 64 * h; c0 < 64 * h + 64; c0 += 32) {
-        float sv[32], dp[32];
-        tmem_ld32(tS + c0, sv);
-        tmem_ld32(tDP + c0, dp);
-        uint32_t pk[16], dk[16];
+        for (int c0 = 64 * h; c0 < 64 * h + 64; c0 += 32) {
+          float sv[32], dp[32];
+          tmem_ld32(tS + c0, sv);
+          tmem_ld32(tDP + c0, dp);
+          uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int q = 0; q < 32; q += 2) {
-          const int qi = c0 + q;
-          const float2 x = __ffma2_rn(make_float2(sv[q], sv[q + 1]), make_float2(c_log2, c_log2),
-                                      make_float2(-vec[qi], -vec[qi + 1]));
-          float p0 = ex2_mufu(x.x), p1 = ex2_mufu(x.y);
-          if (key_dead || (diag && (i * kBTile + qi) < k_glob)) p0 = 0.f;
-          if (key_dead || (diag && (i * kBTile + qi + 1) < k_glob)) p1 = 0.f;
-          const float2 ds = __fmul2_rn(make_float2(p0, p1),
-                                       __fadd2_rn(make_float2(dp[q], dp[q + 1]),
-                                                  make_float2(-vec[kBTile + qi], -vec[kBTile + qi + 1])));
-          pk[q >> 1] = pack_bf16(p0, p1);
-          dk[q >> 1] = pack_bf16(ds.x, ds.y);
+          for (int q = 0; q < 32; q += 4) {
+            // vec holds -LSE2 and -D (negated by the preprocess kernel)
+            const float4 nl = *reinterpret_cast<const float4*>(vec + c0 + q);
+            const float4 nd = *reinterpret_cast<const float4*>(vec + kBTile + c0 + q);
+            const float2 x01 = __ffma2_rn(make_float2(sv[q], sv[q + 1]), make_float2(c_log2, c_log2), make_float2(nl.x, nl.y));
+            const float2 x23 = __ffma2_rn(make_float2(sv[q + 2], sv[q + 3]), make_float2(c_log2, c_log2), make_float2(nl.z, nl.w));
+            float p0 = ex2_mufu(x01.x), p1 = ex2_mufu(x01.y), p2 = ex2_mufu(x23.x), p3 = ex2_mufu(x23.y);
+            if constexpr (decltype(masked)::value) {
+              const int q0 = i * kBTile + c0 + q;  // global query index of p0
+              if (key_dead || (diag && q0 < k_glob)) p0 = 0.f;
+              if (key_dead || (diag && q0 + 1 < k_glob)) p1 = 0.f;
+              if (key_dead || (diag && q0 + 2 < k_glob)) p2 = 0.f;
+              if (key_dead || (diag && q0 + 3 < k_glob)) p3 = 0.f;
+            }
+            const float2 ds01 = __fmul2_rn(make_float2(p0, p1), __fadd2_rn(make_float2(dp[q], dp[q + 1]), make_float2(nd.x, nd.y)));
+            const float2 ds23 = __fmul2_rn(make_float2(p2, p3), __fadd2_rn(make_float2(dp[q + 2], dp[q + 3]), make_float2(nd.z, nd.w)));
+            pk[q >> 1] = pack_bf16(p0, p1);
+            pk[(q >> 1) + 1] = pack_bf16(p2, p3);
+            dk[q >> 1] = pack_bf16(ds01.x, ds01.y);
+            dk[(q >> 1) + 1] = pack_bf16(ds23.x, ds23.y);
+          }
+          // packed bf16 pairs stay inside this warpgroup's half of the columns
+          const int pcol = 64 * h + (c0 % 64) / 2;
+          tmem_st16(tS + pcol, pk);
+          tmem_st16(tDP + pcol, dk);
+          // dS (queries x keys) into shared memory, MN-major with the 128-byte
+          // swizzle: query chunk h at 16 KB, key row lrow at
+          // (lrow/8)*1024 + (lrow%8)*128, 16-byte unit (q%64)/8 xor (lrow%8).
+          uint8_t* ds_row = ds_half + (lrow >> 3) * 1024 + (lrow & 7) * 128;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int unit = ((c0 % 64) / 8 + u) ^ (lrow & 7);
+            *reinterpret_cast<uint4*>(ds_row + unit * 16) =
+                make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+          }
         }
-        // packed bf16 pairs stay inside this warpgroup's half of the columns
-        const int pcol = 64 * h + (c0 % 64) / 2;
-        tmem_st16(tS + pcol, pk);
-        tmem_st16(tDP + pcol, dk);
-        // dS (queries x keys) into shared memory, MN-major with the 128-byte
-        // swizzle: query chunk h at 16 KB, key row lrow at
-        // (lrow/8)*1024 + (lrow%8)*128, 16-byte unit (q%64)/8 xor (lrow%8).
-        uint8_t* ds_row = ds_half + (lrow >> 3) * 1024 + (lrow & 7) * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit = ((c0 % 64) / 8 + u) ^ (lrow & 7);
-          *reinterpret_cast<uint4*>(ds_row + unit * 16) =
-              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-        }
-      }
+      };
+      if (mask_tile) half_tile(std::true_type{});
+      else half_tile(std::false_type{});
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(L::kBarDSFull));
-
-      // ---- dQ_i read-out: this warpgroup's D/2 columns, then FP32 reductions
-      // into the accumulator (the dQ product has also finished reading dS, so
-      // the next tile's dS may be written after this point)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
-      if (!ok) break;
-      tc_fence_after();
-      float dq[D / 2];
-#pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 32) tmem_ld32p(tDQ + c0, dq + c0);
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarDQFree));  // tensor-memory dQ columns may be overwritten
-      // accumulator layout per (bh, i): [D/4 column groups][128 rows][4]; this
-      // warpgroup's groups are h*D/8 .. (h+1)*D/8 - 1.  A warp's 16-byte
-      // reductions to one group cover 512 contiguous bytes.
-      float4* gdst = reinterpret_cast<float4*>(p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile)) +
-                     (size_t)h * (D / 8) * kBTile + lrow;
-      int* ticket = DETERMINISTIC ? p.tickets + ((size_t)bh * p.n_tiles + i) * 2 + h : nullptr;
-      if (DETERMINISTIC) {
-        if (tid == 0) {
-          const uint64_t t0 = globaltimer_ns();
-          while (ld_acquire_gpu(ticket) != j) {  // tile i takes key tiles in ascending j
-            if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
-              if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
-              *ctl.abort = 1;
-              break;
-            }
-          }
-        }
-        named_bar_sync(1 + h, 128);  // every thread's additions come after the acquire
-      }
-      if (!*ctl.abort) {
-#pragma unroll
-        for (int g = 0; g < D / 8; ++g)
-          atomicAdd(gdst + (size_t)g * kBTile, make_float4(dq[4 * g], dq[4 * g + 1], dq[4 * g + 2], dq[4 * g + 3]));
-      }
-      if (DETERMINISTIC) {
-        __threadfence();
-        named_bar_sync(1 + h, 128);
-        if (tid == 0 && !*ctl.abort) red_release_gpu_add(ticket, 1);
-      }
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 7 + h);
     }
     // epilogue: dV and dK rows of this key tile; warpgroup h writes columns
     // [h*D/2, (h+1)*D/2)
@@ -457,6 +460,64 @@ __global__ void __launch_bounds__(320, 1) bwd_kernel(const __grid_constant__ Bwd
           }
         }
       }
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kDqRegs));
+    // ========================== dQ warpgroup ===========================
+    // Reads dQ_i (queries on tensor-memory lanes) as soon as its product is
+    // done, frees those columns, then adds the row into the FP32
+    // accumulator with 16-byte reductions while the other warpgroups move on
+    // to the next query tile.
+    const int quad = warp & 3;
+    const int qrow = quad * 32 + lane;
+    const int tid = threadIdx.x - 384;
+    const uint32_t tDQ = tmem + ((uint32_t)(quad * 32) << 16) + L::kColDQ;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int i = tile_of(it);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
+      if (!ok) break;
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 9);
+      tc_fence_after();
+      float dq[D];
+      if constexpr (D == 128) {  // two 64-column loads, one wait each
+        tmem_ld64(tDQ, *reinterpret_cast<float(*)[64]>(dq));
+        tmem_ld64(tDQ + 64, *reinterpret_cast<float(*)[64]>(dq + 64));
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32p(tDQ + c0, dq + c0);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDQFree));  // tensor-memory dQ columns may be overwritten
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 15);
+      // accumulator layout per (bh, i): [D/4 column groups][128 rows][4]; a
+      // warp's 16-byte reductions to one group cover 512 contiguous bytes
+      float4* gdst = reinterpret_cast<float4*>(p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile)) + qrow;
+      int* ticket = DETERMINISTIC ? p.tickets + (size_t)bh * p.n_tiles + i : nullptr;
+      if (DETERMINISTIC) {
+        if (tid == 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(ticket) != j) {  // tile i takes key tiles in ascending j
+            if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
+              if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
+              *ctl.abort = 1;
+              break;
+            }
+          }
+        }
+        named_bar_sync(1, 128);  // every thread's additions come after the acquire
+      }
+      if (!*ctl.abort) {
+#pragma unroll
+        for (int g = 0; g < D / 4; ++g)
+          atomicAdd(gdst + (size_t)g * kBTile, make_float4(dq[4 * g], dq[4 * g + 1], dq[4 * g + 2], dq[4 * g + 3]));
+      }
+      if (DETERMINISTIC) {
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (tid == 0 && !*ctl.abort) red_release_gpu_add(ticket, 1);
+      }
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 11);
     }
   }
 
@@ -489,6 +550,12 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
     auto kernel = bwd_kernel<D, CAUSAL, DET>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits for registers the dec released: the split must
+    // match what the launch hands out
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != L::kLaunchRegs) return cudaErrorInvalidConfiguration;
     kernel<<<p.BH * p.n_tiles, L::kThreads, L::kSmemBytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

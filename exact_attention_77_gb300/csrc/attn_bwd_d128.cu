@@ -9,3 +9,10 @@ cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, bool deterministic,
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TRACE
+// Debug builds only: copy the phase-trace stamps to host memory.
+extern "C" int attn_debug_trace_read(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, attn::g_attn_trace, bytes) == cudaSuccess ? 0 : 5;
+}
+#endif

@@ -38,10 +38,10 @@ struct BwdParams {
   void* dq;           // bf16 [BH, N, d_qk]
   void* dk;           // bf16 [BH, N, d_qk]
   void* dv;           // bf16 [BH, N, d_v]
-  float* row_lse2;    // workspace fp32 [BH, Npad]: LSE * log2(e), +inf on padding rows
-  float* row_d;       // workspace fp32 [BH, Npad]: rowsum(dO * O), 0 on padding rows
+  float* row_lse2;    // workspace fp32 [BH, Npad]: -LSE * log2(e), -inf on padding rows
+  float* row_d;       // workspace fp32 [BH, Npad]: -rowsum(dO * O), 0 on padding rows
   float* dq_acc;      // workspace fp32 [BH, n_tiles, d_qk/4, 128, 4]
-  int* tickets;       // workspace int32 [BH, n_tiles, 2] (deterministic mode; one per dQ column half)
+  int* tickets;       // workspace int32 [BH, n_tiles] (deterministic mode)
   DeviceStatus* status;
   unsigned long long timeout_ns;
   int N;

@@ -12,6 +12,24 @@
 
 namespace attn {
 
+// ------------------------------------------------------------------ trace
+// Debug builds only (-DATTN_TRACE): clock64 stamps at named points of the
+// first CTAs' first iterations, read back by attn_debug_trace_read.  The
+// library as shipped compiles this away.
+#ifdef ATTN_TRACE
+constexpr int kTraceCtas = 4, kTraceIters = 32, kTracePoints = 16;
+static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceIters * kTracePoints];
+#define ATTN_TRACE_AT(cta, it, pt)                                                         \
+  do {                                                                                     \
+    if ((cta) < kTraceCtas && (it) < kTraceIters)                                          \
+      g_attn_trace[((cta) * kTraceIters + (it)) * kTracePoints + (pt)] = clock64();        \
+  } while (0)
+#else
+#define ATTN_TRACE_AT(cta, it, pt) \
+  do {                             \
+  } while (0)
+#endif
+
 // ----------------------------------------------------------------- status
 // The device status word the host reads with attn_get_device_status.  The
 // first error wins; ``where`` records which wait or check gave up.

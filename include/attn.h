@@ -76,7 +76,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * Bytes of device workspace attn_bwd needs for these sizes (0 for sizes the
  * backward does not accept).  The workspace holds, per (b, h): the FP32 row
  * terms D_i = dO_i . O_i and LSE_i * log2(e) (padded to a multiple of 128
- * rows), the FP32 dQ accumulator, and (deterministic mode) two int32 tickets per
+ * rows), the FP32 dQ accumulator, and (deterministic mode) one int32 ticket per
  * 128-row query tile.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d_qk, int d_v, int deterministic);
