@@ -24,19 +24,18 @@
 //                      dV  += P^T dO_i           (TS, P^T bf16 in tensor memory)
 //                      dK  += dS^T Q_i           (TS, dS^T bf16 in tensor memory)
 //                      dQ_i = dS K_j             (SS, dS bf16 in shared memory)
-//                    and adds dQ_i into the FP32 accumulator with 16-byte
-//                    vector reductions straight from registers (atomic
-//                    mode), or with the same reductions in ascending-j order
-//                    behind a per-(b, h, i) ticket
-//                    (deterministic mode).
+//                    and adds dQ_i into the FP32 accumulator with bulk
+//                    reduce-add copies from a shared-memory staging tile
+//                    (atomic mode), or with the same copies in ascending-j
+//                    order behind a per-(b, h, i) ticket (deterministic mode).
 //   dq_convert_kernel  dQ = scale * accumulator, as bf16 [B,H,N,d].
 //
 // Warp roles in bwd_kernel (512 threads): warp 0 producer (TMA), warp 1 MMA
 // issuer and tensor-memory owner, warps 4-7 and 8-11 two compute warpgroups
 // that split each tile's query columns for the elementwise step (one key row
 // per thread), warps 12-15 the dQ warpgroup (one query row per thread) that
-// reads dQ out of tensor memory and issues its reductions off the critical
-// path.
+// reads dQ out of tensor memory and stages it for the copy engine's
+// reduce-add, off the critical path.
 #pragma once
 
 #include <type_traits>
@@ -52,29 +51,33 @@ constexpr int kBSub = 128 * 128;  // 128 rows x 128 bytes
 template <int D>
 struct BwdLayout {
   static constexpr int kTileBytes = kBTile * D * 2;  // one bf16 [128, D] tile
+  // Q_i / dO_i stages: two at d = 64; one at d = 128, where shared memory
+  // goes to the FP32 dQ staging tile instead (Q_{i+1} and dO_{i+1} are
+  // reloaded as soon as the dK / dV products release them).
+  static constexpr int kStages = D == 64 ? 2 : 1;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
-  static constexpr int kQOff = kVOff + kTileBytes;           // 2 stages
-  static constexpr int kDOOff = kQOff + 2 * kTileBytes;      // 2 stages
-  static constexpr int kDSOff = kDOOff + 2 * kTileBytes;     // dS (bf16 128x128), MN-major for the dQ product
+  static constexpr int kQOff = kVOff + kTileBytes;
+  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
+  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;  // dS (bf16 128x128), MN-major for the dQ product
   static constexpr int kDSBytes = kBTile * kBTile * 2;
-  static constexpr int kVecOff = kDSOff + kDSBytes;          // 2 stages x (LSE2[128], D[128]) fp32
+  static constexpr int kStgOff = kDSOff + kDSBytes;  // dQ_i FP32 staging, [D/4][128][4] like the accumulator
+  static constexpr int kStgBytes = kBTile * D * 4;
+  static constexpr int kVecOff = kStgOff + kStgBytes;  // per stage: -LSE2[128], -D[128] fp32
   static constexpr int kVecBytes = 2 * kBTile * 4;
-  static constexpr int kBarOff = kVecOff + 2 * kVecBytes;
-  enum {
-    kBarKV = 0,
-    kBarQFull = 1,   // +stage
-    kBarQEmpty = 3,
-    kBarDOFull = 5,
-    kBarDOEmpty = 7,
-    kBarSFull = 9,
-    kBarDPFull,
-    kBarDSFull,
-    kBarDQFull,
-    kBarDQFree,
-    kBarAccDone,
-    kNumBars
-  };
+  static constexpr int kBarOff = kVecOff + kStages * kVecBytes;
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarQFull = 1;  // + stage
+  static constexpr int kBarQEmpty = kBarQFull + kStages;
+  static constexpr int kBarDOFull = kBarQEmpty + kStages;
+  static constexpr int kBarDOEmpty = kBarDOFull + kStages;
+  static constexpr int kBarSFull = kBarDOEmpty + kStages;
+  static constexpr int kBarDPFull = kBarSFull + 1;
+  static constexpr int kBarDSFull = kBarDPFull + 1;
+  static constexpr int kBarDQFull = kBarDSFull + 1;
+  static constexpr int kBarDQFree = kBarDQFull + 1;
+  static constexpr int kBarAccDone = kBarDQFree + 1;
+  static constexpr int kNumBars = kBarAccDone + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -244,8 +247,8 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = ((it >> 1) & 1) ^ 1;
+        const int s = it % L::kStages;
+        const uint32_t ph = ((it / L::kStages) & 1) ^ 1;
         const int i = tile_of(it);
         if (!mbar_wait(bar(L::kBarQEmpty + s), ph, ctl, kBWhereProd)) break;
         mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kTileBytes + L::kVecBytes);
@@ -271,9 +274,9 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         issued = it + 1;
       }
       mbar_wait_drain(bar(L::kBarKV), 0, p.timeout_ns);
-      for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it) {
-        mbar_wait_drain(bar(L::kBarQFull + (it & 1)), (it >> 1) & 1, p.timeout_ns);
-        mbar_wait_drain(bar(L::kBarDOFull + (it & 1)), (it >> 1) & 1, p.timeout_ns);
+      for (int it = issued > L::kStages ? issued - L::kStages : 0; it < issued; ++it) {
+        mbar_wait_drain(bar(L::kBarQFull + it % L::kStages), (it / L::kStages) & 1, p.timeout_ns);
+        mbar_wait_drain(bar(L::kBarDOFull + it % L::kStages), (it / L::kStages) & 1, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
@@ -303,8 +306,8 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       bool ok = mbar_wait(bar(L::kBarKV), 0, ctl, kBWhereMma);
       tc_fence_after();
       for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
+        const int s = it % L::kStages;
+        const uint32_t ph = (it / L::kStages) & 1;
         const uint32_t qs = sbase + L::kQOff + s * L::kTileBytes;
         const uint32_t dos = sbase + L::kDOOff + s * L::kTileBytes;
         if (!(ok = mbar_wait(bar(L::kBarQFull + s), ph, ctl, kBWhereMma + 1))) break;
@@ -365,10 +368,10 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     const bool key_dead = k_glob >= p.N;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1;
+      const int s = it % L::kStages;
       const int i = tile_of(it);
       // LSE2 / D vectors arrive with Q_i on the stage's barrier
-      ok = mbar_wait(bar(L::kBarQFull + s), (it >> 1) & 1, ctl, kBWhereEw + 3);
+      ok = mbar_wait(bar(L::kBarQFull + s), (it / L::kStages) & 1, ctl, kBWhereEw + 3);
       ok = ok && mbar_wait(bar(L::kBarSFull), it & 1, ctl, kBWhereEw);
       ok = ok && mbar_wait(bar(L::kBarDPFull), it & 1, ctl, kBWhereEw + 1);
       ok = __all_sync(0xffffffffu, ok);
@@ -465,9 +468,9 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kDqRegs));
     // ========================== dQ warpgroup ===========================
     // Reads dQ_i (queries on tensor-memory lanes) as soon as its product is
-    // done, frees those columns, then adds the row into the FP32
-    // accumulator with 16-byte reductions while the other warpgroups move on
-    // to the next query tile.
+    // done, frees those columns, and has the copy engine add the tile into
+    // the FP32 accumulator while the other warpgroups move on to the next
+    // query tile.
     const int quad = warp & 3;
     const int qrow = quad * 32 + lane;
     const int tid = threadIdx.x - 384;
@@ -490,12 +493,26 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       tc_fence_before();
       mbar_arrive(bar(L::kBarDQFree));  // tensor-memory dQ columns may be overwritten
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 15);
-      // accumulator layout per (bh, i): [D/4 column groups][128 rows][4]; a
-      // warp's 16-byte reductions to one group cover 512 contiguous bytes
-      float4* gdst = reinterpret_cast<float4*>(p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile)) + qrow;
-      int* ticket = DETERMINISTIC ? p.tickets + (size_t)bh * p.n_tiles + i : nullptr;
-      if (DETERMINISTIC) {
-        if (tid == 0) {
+      // Stage the tile in shared memory in the accumulator's [D/4 column
+      // groups][128 rows][4] order (each thread's 16-byte stores land side by
+      // side with its neighbours'), then one thread hands it to the copy
+      // engine as a bulk FP32 reduce-add.  The staging tile is reused once
+      // the previous tile's bulk read of it has finished.
+      float* stg = reinterpret_cast<float*>(smem + L::kStgOff);
+      if (it > 0) {
+        if (tid == 0) bulk_wait_read<0>();
+        named_bar_sync(1, 128);
+      }
+#pragma unroll
+      for (int g = 0; g < D / 4; ++g)
+        *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+            make_float4(dq[4 * g], dq[4 * g + 1], dq[4 * g + 2], dq[4 * g + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (tid == 0) {
+        float* gdst = p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile);
+        int* ticket = DETERMINISTIC ? p.tickets + (size_t)bh * p.n_tiles + i : nullptr;
+        if (DETERMINISTIC) {
           const uint64_t t0 = globaltimer_ns();
           while (ld_acquire_gpu(ticket) != j) {  // tile i takes key tiles in ascending j
             if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
@@ -504,21 +521,22 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
               break;
             }
           }
+          fence_proxy_async_global();
         }
-        named_bar_sync(1, 128);  // every thread's additions come after the acquire
-      }
-      if (!*ctl.abort) {
-#pragma unroll
-        for (int g = 0; g < D / 4; ++g)
-          atomicAdd(gdst + (size_t)g * kBTile, make_float4(dq[4 * g], dq[4 * g + 1], dq[4 * g + 2], dq[4 * g + 3]));
-      }
-      if (DETERMINISTIC) {
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (tid == 0 && !*ctl.abort) red_release_gpu_add(ticket, 1);
+        if (!*ctl.abort) {
+          bulk_reduce_add_f32(gdst, smem_u32(stg), L::kStgBytes / 2);
+          bulk_reduce_add_f32(gdst + D * kBTile / 2, smem_u32(stg + D * kBTile / 2), L::kStgBytes / 2);
+          bulk_commit();
+        }
+        if (DETERMINISTIC) {
+          bulk_wait_all<0>();  // the additions are performed before the next key tile's
+          fence_proxy_async_global();
+          if (!*ctl.abort) red_release_gpu_add(ticket, 1);
+        }
       }
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 11);
     }
+    if (tid == 0) bulk_wait_all<0>();  // staging reads done before the CTA exits
   }
 
   tc_fence_before();
