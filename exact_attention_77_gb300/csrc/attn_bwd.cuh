@@ -51,29 +51,35 @@ constexpr int kBSub = 128 * 128;  // 128 rows x 128 bytes
 template <int D>
 struct BwdLayout {
   static constexpr int kTileBytes = kBTile * D * 2;  // one bf16 [128, D] tile
-  // Q_i / dO_i stages: two at d = 64; one at d = 128, where shared memory
-  // goes to the FP32 dQ staging tile instead (Q_{i+1} and dO_{i+1} are
-  // reloaded as soon as the dK / dV products release them).
-  static constexpr int kStages = D == 64 ? 2 : 1;
+  // Q_i (with its -LSE2 / -D vectors) is double-buffered: the S^T product of
+  // the next tile must not wait for its load.  dO_i is double-buffered at
+  // d = 64; at d = 128 it has one stage (released right after the dV product)
+  // so that 32 KiB stays free for the dQ staging tile.
+  static constexpr int kQStages = 2;
+  static constexpr int kDOStages = D == 64 ? 2 : 1;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;
-  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;  // dS (bf16 128x128), MN-major for the dQ product
+  static constexpr int kDOOff = kQOff + kQStages * kTileBytes;
+  static constexpr int kDSOff = kDOOff + kDOStages * kTileBytes;  // dS (bf16 128x128), MN-major for the dQ product
   static constexpr int kDSBytes = kBTile * kBTile * 2;
-  static constexpr int kStgOff = kDSOff + kDSBytes;  // dQ_i FP32 staging, [D/4][128][4] like the accumulator
-  static constexpr int kStgBytes = kBTile * D * 4;
-  static constexpr int kVecOff = kStgOff + kStgBytes;  // per stage: -LSE2[128], -D[128] fp32
+  // dQ_i FP32 staging in the accumulator's [D/4][128][4] order: 32 KiB, the
+  // whole tile at d = 64, half of it (two rounds) at d = 128
+  static constexpr int kStgOff = kDSOff + kDSBytes;
+  static constexpr int kStgBytes = 32 * 1024;
+  static constexpr int kStgRounds = kBTile * D * 4 / kStgBytes;
+  static constexpr int kVecOff = kStgOff + kStgBytes;  // per Q stage: -LSE2[128], -D[128] fp32
   static constexpr int kVecBytes = 2 * kBTile * 4;
-  static constexpr int kBarOff = kVecOff + kStages * kVecBytes;
+  static constexpr int kBarOff = kVecOff + kQStages * kVecBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;  // + stage
-  static constexpr int kBarQEmpty = kBarQFull + kStages;
-  static constexpr int kBarDOFull = kBarQEmpty + kStages;
-  static constexpr int kBarDOEmpty = kBarDOFull + kStages;
-  static constexpr int kBarSFull = kBarDOEmpty + kStages;
-  static constexpr int kBarDPFull = kBarSFull + 1;
-  static constexpr int kBarDSFull = kBarDPFull + 1;
+  static constexpr int kBarQEmpty = kBarQFull + kQStages;
+  static constexpr int kBarDOFull = kBarQEmpty + kQStages;
+  static constexpr int kBarDOEmpty = kBarDOFull + kDOStages;
+  static constexpr int kBarSFull = kBarDOEmpty + kDOStages;  // S^T in tensor memory (commit)
+  static constexpr int kBarDPFull = kBarSFull + 1;            // dP^T in tensor memory (commit)
+  static constexpr int kBarPReady = kBarDPFull + 1;           // P^T written (256 arrivals)
+  static constexpr int kBarDSFull = kBarPReady + 1;           // dS^T and dS written (256 arrivals)
   static constexpr int kBarDQFull = kBarDSFull + 1;
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarAccDone = kBarDQFree + 1;
@@ -82,18 +88,20 @@ struct BwdLayout {
   static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   // tensor memory columns
-  static constexpr int kColS = 0;      // S^T fp32 [128 x 128]; P^T bf16 packed in columns 0-31 and 64-95
+  // S^T fp32 [128 keys x 128 queries]; warpgroup h packs P^T (bf16) for its
+  // queries 64h .. 64h+63 into columns 64h .. 64h+31, inside the columns it read
+  static constexpr int kColS = 0;
   static constexpr int kColDP = 128;   // dP^T fp32; dS^T bf16 packed the same way
   static constexpr int kColDV = 256;   // dV accumulator [128 x D]
   static constexpr int kColDK = 256 + D;
   static constexpr int kColDQ = D == 64 ? 384 : 0;  // d = 128 shares the S^T columns
   // 16 warps in four warpgroups: control (producer, MMA issuer), two compute
   // warpgroups, one dQ warpgroup.  setmaxnreg split of the 128 registers a
-  // thread gets at launch: 72 * 128 + 144 * 256 + 144 * 128 <= 128 * 512.
+  // thread gets at launch: 112 * 128 + 128 * 256 + 144 * 128 <= 128 * 512.
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;
-  static constexpr int kCtlRegs = 72;
-  static constexpr int kComputeRegs = 144;
+  static constexpr int kCtlRegs = 112;
+  static constexpr int kComputeRegs = 128;
   static constexpr int kDqRegs = 144;
   static_assert(kCtlRegs * 128 + kComputeRegs * 256 + kDqRegs * 128 <= kLaunchRegs * kThreads, "register split");
 };
@@ -214,7 +222,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
   if (threadIdx.x == 0) {
     for (int b = 0; b < L::kNumBars; ++b) {
       uint32_t cnt = 1;
-      if (b == L::kBarDSFull) cnt = 256;  // both compute warpgroups
+      if (b == L::kBarPReady || b == L::kBarDSFull) cnt = 256;  // both compute warpgroups
       if (b == L::kBarDQFree) cnt = 128;  // the dQ warpgroup
       mbar_init(bar(b), cnt);
     }
@@ -245,10 +253,12 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         tma_load_3d(sbase + L::kKOff + c * kBSub, &p.tm_k, c * 64, j * kBTile, bh, bar(L::kBarKV));
         tma_load_3d(sbase + L::kVOff + c * kBSub, &p.tm_v, c * 64, j * kBTile, bh, bar(L::kBarKV));
       }
-      int issued = 0;
+      int issued_q = 0, issued_do = 0;  // loads issued per ring
       for (int it = 0; it < n_it; ++it) {
-        const int s = it % L::kStages;
-        const uint32_t ph = ((it / L::kStages) & 1) ^ 1;
+        const int s = it % L::kQStages;
+        const uint32_t ph = ((it / L::kQStages) & 1) ^ 1;
+        const int sd = it % L::kDOStages;
+        const uint32_t phd = ((it / L::kDOStages) & 1) ^ 1;
         const int i = tile_of(it);
         if (!mbar_wait(bar(L::kBarQEmpty + s), ph, ctl, kBWhereProd)) break;
         mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kTileBytes + L::kVecBytes);
@@ -261,84 +271,93 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         bulk_load(sbase + L::kVecOff + s * L::kVecBytes + kBTile * 4, p.row_d + vrow, kBTile * 4,
                   bar(L::kBarQFull + s));
         ATTN_TRACE_AT(blockIdx.x, it, 13);
-        if (!mbar_wait(bar(L::kBarDOEmpty + s), ph, ctl, kBWhereProd + 1)) {
-          issued = it + 1;
-          break;
-        }
-        mbar_arrive_expect_tx(bar(L::kBarDOFull + s), L::kTileBytes);
+        issued_q = it + 1;
+        if (!mbar_wait(bar(L::kBarDOEmpty + sd), phd, ctl, kBWhereProd + 1)) break;
+        mbar_arrive_expect_tx(bar(L::kBarDOFull + sd), L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sbase + L::kDOOff + s * L::kTileBytes + c * kBSub, &p.tm_do, c * 64, i * kBTile, bh,
-                      bar(L::kBarDOFull + s));
+          tma_load_3d(sbase + L::kDOOff + sd * L::kTileBytes + c * kBSub, &p.tm_do, c * 64, i * kBTile, bh,
+                      bar(L::kBarDOFull + sd));
         ATTN_TRACE_AT(blockIdx.x, it, 14);
-        issued = it + 1;
+        issued_do = it + 1;
       }
+      // loads still in flight land before the CTA exits: each ring's last
+      // (stage count) loads, each on the newest phase of its stage
       mbar_wait_drain(bar(L::kBarKV), 0, p.timeout_ns);
-      for (int it = issued > L::kStages ? issued - L::kStages : 0; it < issued; ++it) {
-        mbar_wait_drain(bar(L::kBarQFull + it % L::kStages), (it / L::kStages) & 1, p.timeout_ns);
-        mbar_wait_drain(bar(L::kBarDOFull + it % L::kStages), (it / L::kStages) & 1, p.timeout_ns);
-      }
+      for (int it = issued_q > L::kQStages ? issued_q - L::kQStages : 0; it < issued_q; ++it)
+        mbar_wait_drain(bar(L::kBarQFull + it % L::kQStages), (it / L::kQStages) & 1, p.timeout_ns);
+      for (int it = issued_do > L::kDOStages ? issued_do - L::kDOStages : 0; it < issued_do; ++it)
+        mbar_wait_drain(bar(L::kBarDOFull + it % L::kDOStages), (it / L::kDOStages) & 1, p.timeout_ns);
     }
+    __syncwarp();  // lanes 1-31 wait for lane 0 before the final barrier
   } else if (warp == 1) {
     // ============================ MMA issuer ===========================
     if (lane == 0) {
       constexpr uint32_t kIdSq = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);    // dV, dK (A in tensor memory)
       constexpr uint32_t kIdDq = idesc_bf16_f32(128, D, true, true);      // dQ (A = dS, MN-major)
-      // C = A B with A [128 x D] K-major at a_base and B [128 x D] K-major at b_base
+      // C = A B^T with A [128 x D] K-major at a_base and B [128 x D] K-major at b_base
       auto mma_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+        const uint64_t da = sdesc_sw128(a_base, 16, 1024);
+        const uint64_t db = sdesc_sw128(b_base, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * kBSub + (kk % 4) * 32;
-          mma_ss(tmem + d_col, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), kIdSq,
-                 kk > 0);
+          mma_ss(tmem + d_col, sdesc_advance(da, off), sdesc_advance(db, off), kIdSq, kk > 0);
         }
       };
       // C (+)= A[tmem, 128 x 128 bf16] B, B = [128 (K) x D] MN-major at b_base.
-      // A's queries 64h..64h+63 sit packed in columns 64h..64h+31 (each
-      // compute warpgroup packs into the half of S^T / dP^T it read).
+      // A's queries 64h..64h+63 sit packed in columns 64h..64h+31.
       auto mma_tmem_a = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base, bool acc) {
+        const uint64_t db = sdesc_sw128(b_base, kBSub, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBTile / 16; ++kk)
-          mma_ts(tmem + d_col, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8,
-                 sdesc_sw128(b_base + kk * 2048, kBSub, 1024), kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + d_col, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8, sdesc_advance(db, kk * 2048), kIdAcc,
+                 (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar(L::kBarKV), 0, ctl, kBWhereMma);
       tc_fence_after();
       for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % L::kStages;
-        const uint32_t ph = (it / L::kStages) & 1;
+        const int s = it % L::kQStages;
+        const uint32_t ph = (it / L::kQStages) & 1;
+        const int sd = it % L::kDOStages;
+        const uint32_t phd = (it / L::kDOStages) & 1;
         const uint32_t qs = sbase + L::kQOff + s * L::kTileBytes;
-        const uint32_t dos = sbase + L::kDOOff + s * L::kTileBytes;
+        const uint32_t dos = sbase + L::kDOOff + sd * L::kTileBytes;
         if (!(ok = mbar_wait(bar(L::kBarQFull + s), ph, ctl, kBWhereMma + 1))) break;
         ATTN_TRACE_AT(blockIdx.x, it, 0);
         if (L::kColDQ == L::kColS && it > 0)  // S^T columns still hold dQ of the previous tile
           if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 2))) break;
         ATTN_TRACE_AT(blockIdx.x, it, 1);
         tc_fence_after();
-        mma_kmajor(L::kColS, sbase + L::kKOff, qs);
+        mma_kmajor(L::kColS, sbase + L::kKOff, qs);  // the compute warpgroups start P on it
         tc_commit(bar(L::kBarSFull));
         ATTN_TRACE_AT(blockIdx.x, it, 10);
-        if (!(ok = mbar_wait(bar(L::kBarDOFull + s), ph, ctl, kBWhereMma + 3))) break;
+        if (!(ok = mbar_wait(bar(L::kBarDOFull + sd), phd, ctl, kBWhereMma + 3))) break;
         ATTN_TRACE_AT(blockIdx.x, it, 2);
         tc_fence_after();
-        mma_kmajor(L::kColDP, sbase + L::kVOff, dos);
+        mma_kmajor(L::kColDP, sbase + L::kVOff, dos);  // runs while P is computed
         tc_commit(bar(L::kBarDPFull));
-        ATTN_TRACE_AT(blockIdx.x, it, 12);
-        if (!(ok = mbar_wait(bar(L::kBarDSFull), it & 1, ctl, kBWhereMma + 4))) break;
+        if (!(ok = mbar_wait(bar(L::kBarPReady), it & 1, ctl, kBWhereMma + 4))) break;
         ATTN_TRACE_AT(blockIdx.x, it, 3);
         tc_fence_after();
-        mma_tmem_a(L::kColDV, L::kColS, dos, it > 0);
+        mma_tmem_a(L::kColDV, L::kColS, dos, it > 0);  // runs while dS is computed
+        tc_commit(bar(L::kBarDOEmpty + sd));            // dO_i's last reader: reload it early
+        if (!(ok = mbar_wait(bar(L::kBarDSFull), it & 1, ctl, kBWhereMma + 6))) break;
+        ATTN_TRACE_AT(blockIdx.x, it, 12);
+        tc_fence_after();
         mma_tmem_a(L::kColDK, L::kColDP, qs, it > 0);
         tc_commit(bar(L::kBarQEmpty + s));
-        tc_commit(bar(L::kBarDOEmpty + s));
         if (L::kColDQ != L::kColS && it > 0)
           if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 5))) break;
         tc_fence_after();
+        {
+          const uint64_t da = sdesc_sw128(sbase + L::kDSOff, kBSub, 1024);
+          const uint64_t db = sdesc_sw128(sbase + L::kKOff, kBSub, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBTile / 16; ++kk)
-          mma_ss(tmem + L::kColDQ, sdesc_sw128(sbase + L::kDSOff + kk * 2048, kBSub, 1024),
-                 sdesc_sw128(sbase + L::kKOff + kk * 2048, kBSub, 1024), kIdDq, kk > 0);
+          for (int kk = 0; kk < kBTile / 16; ++kk)
+            mma_ss(tmem + L::kColDQ, sdesc_advance(da, kk * 2048), sdesc_advance(db, kk * 2048), kIdDq, kk > 0);
+        }
         tc_commit(bar(L::kBarDQFull));
         ATTN_TRACE_AT(blockIdx.x, it, 4);
       }
@@ -350,11 +369,11 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kComputeRegs));
     // ================= two compute warpgroups (h = 0, 1) =================
-    // Warpgroup h owns query columns [64h, 64h + 64) of every tile for the
-    // elementwise step (keys on tensor-memory lanes) and columns
-    // [h*D/2, (h+1)*D/2) of the dV / dK epilogue.  The next tile's dS is only
-    // written after its S^T product completed, and that product was issued
-    // after this tile's dQ product (which reads dS), so the buffer is free.
+    // Warpgroup h takes queries 64h .. 64h+63 of the elementwise steps (keys on
+    // tensor-memory lanes) and writes columns [h*D/2, (h+1)*D/2) of the dV /
+    // dK epilogue.  The next tile's dS is only written after its S^T
+    // product completed, and that product was issued after this tile's dQ
+    // product (which reads dS), so the buffer is free.
     const int h = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int lrow = quad * 32 + lane;      // tensor-memory lane: key row
@@ -363,72 +382,95 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + L::kColS;
     const uint32_t tDP = tmem + lane_base + L::kColDP;
-    uint8_t* ds_half = smem + L::kDSOff + h * kBSub;  // dS query chunk h (queries 64h .. 64h+63)
     const float c_log2 = p.scale_log2;
     const bool key_dead = k_glob >= p.N;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it % L::kStages;
+      const int s = it % L::kQStages;
       const int i = tile_of(it);
       // LSE2 / D vectors arrive with Q_i on the stage's barrier
-      ok = mbar_wait(bar(L::kBarQFull + s), (it / L::kStages) & 1, ctl, kBWhereEw + 3);
-      ok = ok && mbar_wait(bar(L::kBarSFull), it & 1, ctl, kBWhereEw);
-      ok = ok && mbar_wait(bar(L::kBarDPFull), it & 1, ctl, kBWhereEw + 1);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + s), (it / L::kQStages) & 1, ctl, kBWhereEw + 3));
       if (!ok) break;
-      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 5 + h);
-      tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(smem + L::kVecOff + s * L::kVecBytes);
       const bool diag = CAUSAL && i == j;
       // the mask only bites on the diagonal tile and on a ragged last key tile
       const bool mask_tile = diag || (j * kBTile + kBTile > p.N);
-      auto half_tile = [&](auto masked) {
+      // Phase 1 (needs S^T): P = 2^(S^T * scale * log2e - LSE2) for this
+      // warpgroup's 64 queries, kept in FP32 registers and packed as bf16
+      // P^T into columns 64h .. 64h+31 (inside the columns just read).
+      // Phase 2 (needs dP^T): dS = P o (dP - D), packed as dS^T the same way
+      // and written to shared memory as dS for the dQ product.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), it & 1, ctl, kBWhereEw));
+      if (!ok) break;
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 5 + h);
+      tc_fence_after();
+      float pv[64];
+      auto p_chunk = [&](int m, auto masked) {
+        const int c0 = 64 * h + 32 * m;
+        float sv[32];
+        tmem_ld32(tS + c0, sv);
+        uint32_t pk[16];
 #pragma unroll
-        for (int c0 = 64 * h; c0 < 64 * h + 64; c0 += 32) {
-          float sv[32], dp[32];
-          tmem_ld32(tS + c0, sv);
-          tmem_ld32(tDP + c0, dp);
-          uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int q = 0; q < 32; q += 4) {
-            // vec holds -LSE2 and -D (negated by the preprocess kernel)
-            const float4 nl = *reinterpret_cast<const float4*>(vec + c0 + q);
-            const float4 nd = *reinterpret_cast<const float4*>(vec + kBTile + c0 + q);
-            const float2 x01 = __ffma2_rn(make_float2(sv[q], sv[q + 1]), make_float2(c_log2, c_log2), make_float2(nl.x, nl.y));
-            const float2 x23 = __ffma2_rn(make_float2(sv[q + 2], sv[q + 3]), make_float2(c_log2, c_log2), make_float2(nl.z, nl.w));
-            float p0 = ex2_mufu(x01.x), p1 = ex2_mufu(x01.y), p2 = ex2_mufu(x23.x), p3 = ex2_mufu(x23.y);
-            if constexpr (decltype(masked)::value) {
-              const int q0 = i * kBTile + c0 + q;  // global query index of p0
-              if (key_dead || (diag && q0 < k_glob)) p0 = 0.f;
-              if (key_dead || (diag && q0 + 1 < k_glob)) p1 = 0.f;
-              if (key_dead || (diag && q0 + 2 < k_glob)) p2 = 0.f;
-              if (key_dead || (diag && q0 + 3 < k_glob)) p3 = 0.f;
-            }
-            const float2 ds01 = __fmul2_rn(make_float2(p0, p1), __fadd2_rn(make_float2(dp[q], dp[q + 1]), make_float2(nd.x, nd.y)));
-            const float2 ds23 = __fmul2_rn(make_float2(p2, p3), __fadd2_rn(make_float2(dp[q + 2], dp[q + 3]), make_float2(nd.z, nd.w)));
-            pk[q >> 1] = pack_bf16(p0, p1);
-            pk[(q >> 1) + 1] = pack_bf16(p2, p3);
-            dk[q >> 1] = pack_bf16(ds01.x, ds01.y);
-            dk[(q >> 1) + 1] = pack_bf16(ds23.x, ds23.y);
+        for (int q = 0; q < 32; q += 4) {
+          const float4 nl = *reinterpret_cast<const float4*>(vec + c0 + q);  // -LSE2 (negated upstream)
+          const float2 x01 = __ffma2_rn(make_float2(sv[q], sv[q + 1]), make_float2(c_log2, c_log2), make_float2(nl.x, nl.y));
+          const float2 x23 = __ffma2_rn(make_float2(sv[q + 2], sv[q + 3]), make_float2(c_log2, c_log2), make_float2(nl.z, nl.w));
+          float p0 = ex2_mufu(x01.x), p1 = ex2_mufu(x01.y), p2 = ex2_mufu(x23.x), p3 = ex2_mufu(x23.y);
+          if constexpr (decltype(masked)::value) {
+            const int q0 = i * kBTile + c0 + q;  // global query index of p0
+            if (key_dead || (diag && q0 < k_glob)) p0 = 0.f;
+            if (key_dead || (diag && q0 + 1 < k_glob)) p1 = 0.f;
+            if (key_dead || (diag && q0 + 2 < k_glob)) p2 = 0.f;
+            if (key_dead || (diag && q0 + 3 < k_glob)) p3 = 0.f;
           }
-          // packed bf16 pairs stay inside this warpgroup's half of the columns
-          const int pcol = 64 * h + (c0 % 64) / 2;
-          tmem_st16(tS + pcol, pk);
-          tmem_st16(tDP + pcol, dk);
-          // dS (queries x keys) into shared memory, MN-major with the 128-byte
-          // swizzle: query chunk h at 16 KB, key row lrow at
-          // (lrow/8)*1024 + (lrow%8)*128, 16-byte unit (q%64)/8 xor (lrow%8).
-          uint8_t* ds_row = ds_half + (lrow >> 3) * 1024 + (lrow & 7) * 128;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int unit = ((c0 % 64) / 8 + u) ^ (lrow & 7);
-            *reinterpret_cast<uint4*>(ds_row + unit * 16) =
-                make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-          }
+          pv[32 * m + q] = p0;
+          pv[32 * m + q + 1] = p1;
+          pv[32 * m + q + 2] = p2;
+          pv[32 * m + q + 3] = p3;
+          pk[q >> 1] = pack_bf16(p0, p1);
+          pk[(q >> 1) + 1] = pack_bf16(p2, p3);
         }
+        tmem_st16(tS + 64 * h + 16 * m, pk);
       };
-      if (mask_tile) half_tile(std::true_type{});
-      else half_tile(std::false_type{});
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        if (mask_tile) p_chunk(m, std::true_type{});
+        else p_chunk(m, std::false_type{});
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarPReady));
+
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), it & 1, ctl, kBWhereEw + 1));
+      if (!ok) break;
+      tc_fence_after();
+      // dS (queries x keys) into shared memory, MN-major with the 128-byte
+      // swizzle: query chunk h at 16 KB, key row lrow at
+      // (lrow/8)*1024 + (lrow%8)*128, 16-byte unit (q%64)/8 xor (lrow%8).
+      uint8_t* ds_row = smem + L::kDSOff + h * kBSub + (lrow >> 3) * 1024 + (lrow & 7) * 128;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int c0 = 64 * h + 32 * m;
+        float dp[32];
+        tmem_ld32(tDP + c0, dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float4 nd = *reinterpret_cast<const float4*>(vec + kBTile + c0 + q);  // -D (negated upstream)
+          const float2 ds01 = __fmul2_rn(make_float2(pv[32 * m + q], pv[32 * m + q + 1]),
+                                         __fadd2_rn(make_float2(dp[q], dp[q + 1]), make_float2(nd.x, nd.y)));
+          const float2 ds23 = __fmul2_rn(make_float2(pv[32 * m + q + 2], pv[32 * m + q + 3]),
+                                         __fadd2_rn(make_float2(dp[q + 2], dp[q + 3]), make_float2(nd.z, nd.w)));
+          dk[q >> 1] = pack_bf16(ds01.x, ds01.y);
+          dk[(q >> 1) + 1] = pack_bf16(ds23.x, ds23.y);
+        }
+        tmem_st16(tDP + 64 * h + 16 * m, dk);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (4 * m + u) ^ (lrow & 7);
+          *reinterpret_cast<uint4*>(ds_row + unit * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -499,44 +541,53 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       // engine as a bulk FP32 reduce-add.  The staging tile is reused once
       // the previous tile's bulk read of it has finished.
       float* stg = reinterpret_cast<float*>(smem + L::kStgOff);
-      if (it > 0) {
-        if (tid == 0) bulk_wait_read<0>();
-        named_bar_sync(1, 128);
-      }
+      float* gdst = p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile);
+      int* ticket = DETERMINISTIC ? p.tickets + (size_t)bh * p.n_tiles + i : nullptr;
+      constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
 #pragma unroll
-      for (int g = 0; g < D / 4; ++g)
-        *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
-            make_float4(dq[4 * g], dq[4 * g + 1], dq[4 * g + 2], dq[4 * g + 3]);
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (tid == 0) {
-        float* gdst = p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile);
-        int* ticket = DETERMINISTIC ? p.tickets + (size_t)bh * p.n_tiles + i : nullptr;
-        if (DETERMINISTIC) {
-          const uint64_t t0 = globaltimer_ns();
-          while (ld_acquire_gpu(ticket) != j) {  // tile i takes key tiles in ascending j
-            if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
-              if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
-              *ctl.abort = 1;
-              break;
+      for (int r = 0; r < L::kStgRounds; ++r) {
+        if (it > 0 || r > 0) {  // the previous round's bulk read of the staging tile
+          if (tid == 0) bulk_wait_read<0>();
+          __syncwarp();
+          named_bar_sync(1, 128);
+        }
+#pragma unroll
+        for (int g = 0; g < kGroupsPerRound; ++g) {
+          const int gg = r * kGroupsPerRound + g;
+          *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+              make_float4(dq[4 * gg], dq[4 * gg + 1], dq[4 * gg + 2], dq[4 * gg + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (tid == 0) {
+          if (DETERMINISTIC && r == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(ticket) != j) {  // tile i takes key tiles in ascending j
+              if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
+                if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
+                *ctl.abort = 1;
+                break;
+              }
             }
+            fence_proxy_async_global();
           }
-          fence_proxy_async_global();
+          if (!*ctl.abort) {
+            bulk_reduce_add_f32(gdst + (size_t)r * kGroupsPerRound * kBTile * 4, smem_u32(stg), L::kStgBytes);
+            bulk_commit();
+          }
         }
-        if (!*ctl.abort) {
-          bulk_reduce_add_f32(gdst, smem_u32(stg), L::kStgBytes / 2);
-          bulk_reduce_add_f32(gdst + D * kBTile / 2, smem_u32(stg + D * kBTile / 2), L::kStgBytes / 2);
-          bulk_commit();
-        }
-        if (DETERMINISTIC) {
-          bulk_wait_all<0>();  // the additions are performed before the next key tile's
-          fence_proxy_async_global();
-          if (!*ctl.abort) red_release_gpu_add(ticket, 1);
-        }
+        __syncwarp();  // lane 0 rejoins its warp before the next (aligned) named barrier
       }
+      if (DETERMINISTIC && tid == 0) {
+        bulk_wait_all<0>();  // the additions are performed before the next key tile's
+        fence_proxy_async_global();
+        if (!*ctl.abort) red_release_gpu_add(ticket, 1);
+      }
+      __syncwarp();
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 11);
     }
     if (tid == 0) bulk_wait_all<0>();  // staging reads done before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       for (int ld = issued > L::kStages ? issued - L::kStages : 0; ld < issued; ++ld)
         mbar_wait_drain(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1, p.timeout_ns);
     }
+    __syncwarp();  // lanes 1-31 wait for lane 0 before the final barrier
   } else if (warp == 1) {
     // =========================== MMA issuer =========================
     if (lane == 0) {
