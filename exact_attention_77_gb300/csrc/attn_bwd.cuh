@@ -94,7 +94,10 @@ struct BwdLayout {
   static constexpr int kColDP = 128;   // dP^T fp32; dS^T bf16 packed the same way
   static constexpr int kColDV = 256;   // dV accumulator [128 x D]
   static constexpr int kColDK = 256 + D;
-  static constexpr int kColDQ = D == 64 ? 384 : 0;  // d = 128 shares the S^T columns
+  // dQ: its own columns at d = 64; at d = 128 it shares the dP^T columns, so
+  // the next tile's S^T can start right after the dQ product and only dP^T
+  // waits for the dQ read-out
+  static constexpr int kColDQ = D == 64 ? 384 : 128;
   // 16 warps in four warpgroups: control (producer, MMA issuer), two compute
   // warpgroups, one dQ warpgroup.  setmaxnreg split of the 128 registers a
   // thread gets at launch: 112 * 128 + 128 * 256 + 144 * 128 <= 128 * 512.
@@ -326,15 +329,15 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         const uint32_t dos = sbase + L::kDOOff + sd * L::kTileBytes;
         if (!(ok = mbar_wait(bar(L::kBarQFull + s), ph, ctl, kBWhereMma + 1))) break;
         ATTN_TRACE_AT(blockIdx.x, it, 0);
-        if (L::kColDQ == L::kColS && it > 0)  // S^T columns still hold dQ of the previous tile
-          if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 2))) break;
-        ATTN_TRACE_AT(blockIdx.x, it, 1);
         tc_fence_after();
         mma_kmajor(L::kColS, sbase + L::kKOff, qs);  // the compute warpgroups start P on it
         tc_commit(bar(L::kBarSFull));
         ATTN_TRACE_AT(blockIdx.x, it, 10);
         if (!(ok = mbar_wait(bar(L::kBarDOFull + sd), phd, ctl, kBWhereMma + 3))) break;
         ATTN_TRACE_AT(blockIdx.x, it, 2);
+        if (L::kColDQ == L::kColDP && it > 0)  // dP^T columns still hold dQ of the previous tile
+          if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 2))) break;
+        ATTN_TRACE_AT(blockIdx.x, it, 1);
         tc_fence_after();
         mma_kmajor(L::kColDP, sbase + L::kVOff, dos);  // runs while P is computed
         tc_commit(bar(L::kBarDPFull));
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         tc_fence_after();
         mma_tmem_a(L::kColDK, L::kColDP, qs, it > 0);
         tc_commit(bar(L::kBarQEmpty + s));
-        if (L::kColDQ != L::kColS && it > 0)
+        if (L::kColDQ != L::kColDP && it > 0)
           if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 5))) break;
         tc_fence_after();
         {
@@ -371,9 +374,9 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     // ================= two compute warpgroups (h = 0, 1) =================
     // Warpgroup h takes queries 64h .. 64h+63 of the elementwise steps (keys on
     // tensor-memory lanes) and writes columns [h*D/2, (h+1)*D/2) of the dV /
-    // dK epilogue.  The next tile's dS is only written after its S^T
-    // product completed, and that product was issued after this tile's dQ
-    // product (which reads dS), so the buffer is free.
+    // dK epilogue.  The next tile's dS is only written after its dP^T product
+    // completed, and that product was issued after this tile's dQ product
+    // (which reads dS), so the buffer is free.
     const int h = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int lrow = quad * 32 + lane;      // tensor-memory lane: key row
