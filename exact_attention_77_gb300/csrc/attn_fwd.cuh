@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
             break;
           }
           const uint32_t dst = sbase + L::kKVOff + s * L::kStageBytes;
+          ATTN_TRACE_AT(blockIdx.x, j, 13 + h);
           if (h == 0) {
             mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
 #pragma unroll
@@ -201,76 +202,123 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     __syncwarp();  // lanes 1-31 wait for lane 0 before the final barrier
   } else if (warp == 1) {
     // =========================== MMA issuer =========================
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, false, true);
-      auto wait_load = [&](int ld) -> bool {
-        const bool r = mbar_wait(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1, ctl, kWhereMmaKV);
-        tc_fence_after();
-        return r;
-      };
-      auto issue_qk = [&](int t, int stage) {
-        const uint64_t da = sdesc_sw128(sbase + t * L::kQBytes, 16, 1024);
-        const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, 16, 1024);
+    // The whole warp runs this loop in step (waits included); one elected
+    // lane issues every product and commit.
+    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, false, true);
+    auto wait_all = [&](uint32_t b, uint32_t parity, int where) -> bool {
+      const bool r = __all_sync(0xffffffffu, mbar_wait(b, parity, ctl, where));
+      tc_fence_after();
+      return r;
+    };
+    auto wait_load = [&](int ld) -> bool {
+      return wait_all(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1, kWhereMmaKV);
+    };
+    auto issue_qk = [&](int t, int stage) {
+      const uint64_t da = sdesc_sw128(sbase + t * L::kQBytes, 16, 1024);
+      const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = (kk / 4) * kSubTile + (kk % 4) * 32;
-          mma_ss(tmem + t * 256, sdesc_advance(da, off), sdesc_advance(db, off), kIdescQK, kk > 0);
+      for (int kk = 0; kk < DQK / 16; ++kk) {
+        const uint32_t off = (kk / 4) * kSubTile + (kk % 4) * 32;
+        mma_ss_elect(tmem + t * 256, sdesc_advance(da, off), sdesc_advance(db, off), kIdescQK, kk > 0);
+      }
+    };
+    auto issue_pv = [&](int t, int stage, bool acc) {
+      const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, kSubTile, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_ts_elect(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * 2048), kIdescPV,
+                     (acc || kk > 0) ? 1u : 0u);
+    };
+    bool ok = wait_all(bar(L::kBarQFull), 0, kWhereMmaQ);
+    if (ok && nkv_max > 0) {
+      ok = wait_load(0);
+      if (ok) {
+#pragma unroll
+        for (int t = 0; t < NQT; ++t)
+          if (nkv[t] > 0) {
+            issue_qk(t, 0);
+            tc_commit_elect(bar(L::kBarSFull + t));
+          }
+        tc_commit_elect(bar(L::kBarKVEmpty + 0));
+      }
+    }
+    for (int j = 0; ok && j < nkv_max; ++j) {
+      const int ldv = 2 * j + 1;
+      const int ldk = 2 * j + 2;
+      if (!(ok = wait_load(ldv))) break;
+      if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 0);
+      bool k_ready = false;
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) {
+        if (ok && j < nkv[t]) {
+          ok = wait_all(bar(L::kBarPFull + t), j & 1, kWhereMmaP);
+          if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 1 + 4 * t);
+          if (ok) {
+            issue_pv(t, ldv % L::kStages, j > 0);
+            tc_commit_elect(bar(L::kBarODone + t));
+            if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 2 + 4 * t);
+          }
         }
-      };
-      auto issue_pv = [&](int t, int stage, bool acc) {
-        const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, kSubTile, 1024);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * 2048), kIdescPV,
-                 (acc || kk > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(bar(L::kBarQFull), 0, ctl, kWhereMmaQ);
-      if (ok && nkv_max > 0) {
-        ok = wait_load(0);
-        if (ok) {
-#pragma unroll
-          for (int t = 0; t < NQT; ++t)
-            if (nkv[t] > 0) {
-              issue_qk(t, 0);
-              tc_commit(bar(L::kBarSFull + t));
-            }
-          tc_commit(bar(L::kBarKVEmpty + 0));
+        if (ok && j + 1 < nkv[t]) {
+          if (!k_ready) {
+            ok = k_ready = wait_load(ldk);
+            if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 3);
+          }
+          if (ok) {
+            issue_qk(t, ldk % L::kStages);
+            tc_commit_elect(bar(L::kBarSFull + t));
+            if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 4 + 4 * t);
+          }
         }
       }
-      for (int j = 0; ok && j < nkv_max; ++j) {
-        const int ldv = 2 * j + 1;
-        const int ldk = 2 * j + 2;
-        if (!(ok = wait_load(ldv))) break;
-        bool k_ready = false;
-#pragma unroll
+      if (!ok) break;
+      tc_commit_elect(bar(L::kBarKVEmpty + ldv % L::kStages));
+      if (k_ready) tc_commit_elect(bar(L::kBarKVEmpty + ldk % L::kStages));
+    }
+    // every product issued above completes before tensor memory is freed
+    tc_commit_elect(bar(L::kBarMmaDone));
+    mbar_wait_drain(bar(L::kBarMmaDone), 0, p.timeout_ns);
+    __syncwarp();
+   }
+#ifdef ATTN_TRACE
+   else if (warp == 2) {
+    // debug only: completion times of the product groups, seen by polling
+    if (lane == 0 && blockIdx.x < kTraceCtas) {
+      bool live = true;
+      auto seen = [&](uint32_t b, uint32_t par) {
+        for (int i = 0; live && i < (1 << 22); ++i)
+          if (mbar_test(b, par)) return;
+        live = false;
+      };
+      for (int j = 0; live && j < nkv_max && j < kTraceIters; ++j)
         for (int t = 0; t < NQT; ++t) {
-          if (ok && j < nkv[t]) {
-            ok = mbar_wait(bar(L::kBarPFull + t), j & 1, ctl, kWhereMmaP);
-            tc_fence_after();
-            if (ok) {
-              issue_pv(t, ldv % L::kStages, j > 0);
-              tc_commit(bar(L::kBarODone + t));
-            }
+          if (j < nkv[t]) {
+            seen(bar(L::kBarODone + t), j & 1);
+            ATTN_TRACE_AT(blockIdx.x, j, 16 + 2 * t);
           }
-          if (ok && j + 1 < nkv[t]) {
-            if (!k_ready) ok = k_ready = wait_load(ldk);
-            if (ok) {
-              issue_qk(t, ldk % L::kStages);
-              tc_commit(bar(L::kBarSFull + t));
-            }
+          if (j + 1 < nkv[t]) {
+            seen(bar(L::kBarSFull + t), (j + 1) & 1);
+            ATTN_TRACE_AT(blockIdx.x, j, 17 + 2 * t);
           }
         }
-        if (!ok) break;
-        tc_commit(bar(L::kBarKVEmpty + ldv % L::kStages));
-        if (k_ready) tc_commit(bar(L::kBarKVEmpty + ldk % L::kStages));
+    }
+    __syncwarp();
+   } else if (warp == 3) {
+    // debug only: landing times of the K_j / V_j tiles
+    if (lane == 0 && blockIdx.x < kTraceCtas) {
+      bool live = true;
+      for (int ld = 0; live && ld < 2 * nkv_max && ld / 2 < kTraceIters; ++ld) {
+        int i = 0;
+        for (; i < (1 << 22); ++i)
+          if (mbar_test(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1)) break;
+        live = i < (1 << 22);
+        ATTN_TRACE_AT(blockIdx.x, ld / 2, 20 + (ld & 1));
       }
-      // every product issued above completes before tensor memory is freed
-      tc_commit(bar(L::kBarMmaDone));
-      mbar_wait_drain(bar(L::kBarMmaDone), 0, p.timeout_ns);
     }
     __syncwarp();
    }
+#endif
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kSmRegs));
     // ====================== softmax warpgroups =======================
@@ -289,6 +337,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     for (int j = 0; j < n; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), j & 1, ctl, kWhereSmS));
       if (!ok) break;
+      if (quad == 0 && lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 9 + 2 * t);
       tc_fence_after();
       float s[128];
       if constexpr (NQT == 1) {  // 128 registers per thread: load in 32-column pieces
@@ -313,6 +362,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       for (int c = 16; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      if (t == 0 && quad == 0 && lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 15);
       const float m_new = fmaxf(m, mx * c_log2);
       const bool need = m_new > m + p.tau;
       if (__any_sync(0xffffffffu, need)) {
@@ -359,6 +409,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + t));
+      if (quad == 0 && lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 10 + 2 * t);
     }
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), (n - 1) & 1, ctl, kWhereSmFinal));

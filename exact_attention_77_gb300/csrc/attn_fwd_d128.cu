@@ -13,3 +13,10 @@ cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, int nqt, int poly, 
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TRACE
+// Debug builds only: copy the forward's phase-trace stamps to host memory.
+extern "C" int attn_debug_trace_read_fwd(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, attn::g_attn_trace, bytes) == cudaSuccess ? 0 : 5;
+}
+#endif

@@ -17,7 +17,7 @@ namespace attn {
 // first CTAs' first iterations, read back by attn_debug_trace_read.  The
 // library as shipped compiles this away.
 #ifdef ATTN_TRACE
-constexpr int kTraceCtas = 4, kTraceIters = 32, kTracePoints = 16;
+constexpr int kTraceCtas = 4, kTraceIters = 32, kTracePoints = 32;
 static __device__ unsigned long long g_attn_trace[kTraceCtas * kTraceIters * kTracePoints];
 #define ATTN_TRACE_AT(cta, it, pt)                                                         \
   do {                                                                                     \
@@ -81,6 +81,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking check whether the phase of ``bar`` with the given parity has
+// completed (acquire semantics when it has).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Per-CTA control block for bounded waits: once any role gives up, the
 // shared abort flag makes every other wait give up too, so all roles reach
 // the teardown (TMEM release) instead of hanging.
@@ -113,6 +127,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 // products already in flight are still waited for) but gives up after
 // ``timeout_ns``.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_test(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (globaltimer_ns() - t0 <= timeout_ns) {
@@ -220,6 +235,45 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Forms for issue loops that the whole warp runs in step: every lane computes
+// the same operands and elect.sync picks the one lane that issues (the lowest
+// active lane, the same one every time in a converged warp; a commit tracks
+// the products of its own thread, so products and commits must share it).
+// Measured on GB300: with the issue loop in a single-lane branch, or with the
+// issuing lane chosen by a lane-index predicate, the issuing warp loses most
+// of its issue slots to the busy softmax warps on the same scheduler and the
+// tensor pipe runs dry; with elect.sync the forward went from about 1330 to
+// about 1700 TFLOP/s.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
