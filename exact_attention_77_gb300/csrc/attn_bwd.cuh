@@ -369,6 +369,32 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     }
     __syncwarp();
    }
+#ifdef ATTN_TRACE
+   else if (warp == 2) {
+    // debug only: completion times of the products, seen by polling
+    if (lane == 0 && blockIdx.x < kTraceCtas) {
+      bool live = true;
+      auto seen = [&](uint32_t b, uint32_t par) {
+        for (int i = 0; live && i < (1 << 22); ++i)
+          if (mbar_test(b, par)) return;
+        live = false;
+      };
+      for (int it = 0; live && it < n_it && it < kTraceIters; ++it) {
+        seen(bar(L::kBarSFull), it & 1);
+        ATTN_TRACE_AT(blockIdx.x, it, 16);
+        seen(bar(L::kBarDPFull), it & 1);
+        ATTN_TRACE_AT(blockIdx.x, it, 17);
+        seen(bar(L::kBarDOEmpty + it % L::kDOStages), (it / L::kDOStages) & 1);
+        ATTN_TRACE_AT(blockIdx.x, it, 18);
+        seen(bar(L::kBarQEmpty + it % L::kQStages), (it / L::kQStages) & 1);
+        ATTN_TRACE_AT(blockIdx.x, it, 19);
+        seen(bar(L::kBarDQFull), it & 1);
+        ATTN_TRACE_AT(blockIdx.x, it, 20);
+      }
+    }
+    __syncwarp();
+   }
+#endif
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kComputeRegs));
     // ================= two compute warpgroups (h = 0, 1) =================
