@@ -78,9 +78,11 @@ struct BwdLayout {
   static constexpr int kBarDOEmpty = kBarDOFull + kDOStages;
   static constexpr int kBarSFull = kBarDOEmpty + kDOStages;  // S^T in tensor memory (commit)
   static constexpr int kBarDPFull = kBarSFull + 1;            // dP^T in tensor memory (commit)
-  static constexpr int kBarPReady = kBarDPFull + 1;           // P^T written (256 arrivals)
-  static constexpr int kBarDSFull = kBarPReady + 1;           // dS^T and dS written (256 arrivals)
-  static constexpr int kBarDQFull = kBarDSFull + 1;
+  // + half m: P^T of queries 64h+32m .. 64h+32m+31 of both warpgroups h
+  // written (256 arrivals); the dV product starts on the first half
+  static constexpr int kBarPReady = kBarDPFull + 1;
+  static constexpr int kBarDSFull = kBarPReady + 2;  // + half m: dS^T and dS, the same way
+  static constexpr int kBarDQFull = kBarDSFull + 2;
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarAccDone = kBarDQFree + 1;
   static constexpr int kNumBars = kBarAccDone + 1;
@@ -225,7 +227,8 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
   if (threadIdx.x == 0) {
     for (int b = 0; b < L::kNumBars; ++b) {
       uint32_t cnt = 1;
-      if (b == L::kBarPReady || b == L::kBarDSFull) cnt = 256;  // both compute warpgroups
+      if ((b >= L::kBarPReady && b < L::kBarPReady + 2) || (b >= L::kBarDSFull && b < L::kBarDSFull + 2))
+        cnt = 256;  // both compute warpgroups
       if (b == L::kBarDQFree) cnt = 128;  // the dQ warpgroup
       mbar_init(bar(b), cnt);
     }
@@ -310,13 +313,18 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         }
       };
       // C (+)= A[tmem, 128 x 128 bf16] B, B = [128 (K) x D] MN-major at b_base.
-      // A's queries 64h..64h+63 sit packed in columns 64h..64h+31.
-      auto mma_tmem_a = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base, bool acc) {
+      // A's queries 64h..64h+63 sit packed in columns 64h..64h+31.  Half m
+      // takes the K steps of queries 64h+32m .. 64h+32m+31 (h = 0, 1).
+      auto mma_tmem_a_half = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base, bool acc, int m) {
         const uint64_t db = sdesc_sw128(b_base, kBSub, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBTile / 16; ++kk)
-          mma_ts(tmem + d_col, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8, sdesc_advance(db, kk * 2048), kIdAcc,
-                 (acc || kk > 0) ? 1u : 0u);
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int kk = 4 * hh + 2 * m + u;
+            mma_ts(tmem + d_col, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8, sdesc_advance(db, kk * 2048), kIdAcc,
+                   (acc || m > 0 || hh > 0 || u > 0) ? 1u : 0u);
+          }
       };
       bool ok = mbar_wait(bar(L::kBarKV), 0, ctl, kBWhereMma);
       tc_fence_after();
@@ -341,15 +349,24 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         tc_fence_after();
         mma_kmajor(L::kColDP, sbase + L::kVOff, dos);  // runs while P is computed
         tc_commit(bar(L::kBarDPFull));
-        if (!(ok = mbar_wait(bar(L::kBarPReady), it & 1, ctl, kBWhereMma + 4))) break;
-        ATTN_TRACE_AT(blockIdx.x, it, 3);
-        tc_fence_after();
-        mma_tmem_a(L::kColDV, L::kColS, dos, it > 0);  // runs while dS is computed
-        tc_commit(bar(L::kBarDOEmpty + sd));            // dO_i's last reader: reload it early
-        if (!(ok = mbar_wait(bar(L::kBarDSFull), it & 1, ctl, kBWhereMma + 6))) break;
-        ATTN_TRACE_AT(blockIdx.x, it, 12);
-        tc_fence_after();
-        mma_tmem_a(L::kColDK, L::kColDP, qs, it > 0);
+        // dV on each half of P^T as it lands (runs while dS is computed)
+#pragma unroll
+        for (int m = 0; m < 2 && ok; ++m) {
+          if (!(ok = mbar_wait(bar(L::kBarPReady + m), it & 1, ctl, kBWhereMma + 4))) break;
+          if (m == 0) ATTN_TRACE_AT(blockIdx.x, it, 3);
+          tc_fence_after();
+          mma_tmem_a_half(L::kColDV, L::kColS, dos, it > 0, m);
+        }
+        if (!ok) break;
+        tc_commit(bar(L::kBarDOEmpty + sd));  // dO_i's last reader: reload it early
+#pragma unroll
+        for (int m = 0; m < 2 && ok; ++m) {
+          if (!(ok = mbar_wait(bar(L::kBarDSFull + m), it & 1, ctl, kBWhereMma + 6))) break;
+          if (m == 0) ATTN_TRACE_AT(blockIdx.x, it, 12);
+          tc_fence_after();
+          mma_tmem_a_half(L::kColDK, L::kColDP, qs, it > 0, m);
+        }
+        if (!ok) break;
         tc_commit(bar(L::kBarQEmpty + s));
         if (L::kColDQ != L::kColDP && it > 0)
           if (!(ok = mbar_wait(bar(L::kBarDQFree), (it - 1) & 1, ctl, kBWhereMma + 5))) break;
@@ -465,10 +482,10 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       for (int m = 0; m < 2; ++m) {
         if (mask_tile) p_chunk(m, std::true_type{});
         else p_chunk(m, std::false_type{});
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarPReady + m));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarPReady));
 
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), it & 1, ctl, kBWhereEw + 1));
       if (!ok) break;
@@ -499,11 +516,11 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
           const int unit = (4 * m + u) ^ (lrow & 7);
           *reinterpret_cast<uint4*>(ds_row + unit * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDSFull + m));
       }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarDSFull));
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 7 + h);
     }
     // epilogue: dV and dK rows of this key tile; warpgroup h writes columns
