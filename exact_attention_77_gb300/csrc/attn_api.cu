@@ -25,6 +25,8 @@ struct Settings {
   unsigned long long timeout_ns = 5ull * 1000 * 1000 * 1000;
   int fwd_tiles = 2;  // query tiles per forward CTA (d = 64 / 128)
   int fwd_poly = 0;   // 1: a share of the exponentials on the FMA-pipe polynomial
+  int fwd_max_ctas = 0;  // persistent forward grid size (0: one CTA per free SM slot)
+  int fwd_persist = -1;  // -1: by sequence length; 0 / 1 forces
   float tau = 8.0f;
   unsigned long long* rescale_counter = nullptr;
 };
@@ -70,6 +72,8 @@ Settings settings() {
       if (v == 1 || v == 2) g_settings.fwd_tiles = v;
     }
     if (const char* e = getenv("ATTN_EXP_POLY")) g_settings.fwd_poly = atoi(e) != 0;
+    if (const char* e = getenv("ATTN_FWD_MAX_CTAS")) g_settings.fwd_max_ctas = atoi(e);
+    if (const char* e = getenv("ATTN_FWD_PERSIST")) g_settings.fwd_persist = atoi(e);
   }
   return g_settings;
 }
@@ -209,6 +213,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.n_qtiles = (N + 127) / 128;
   const int nqt = d_qk == 192 ? 2 : cfg.fwd_tiles;
   p.n_blocks = BH * ((p.n_qtiles + nqt - 1) / nqt);
+  p.max_ctas = cfg.fwd_max_ctas;
+  // short units (N <= 4096: at most 32 K/V tiles each) run persistent
+  p.persist = cfg.fwd_persist >= 0 ? cfg.fwd_persist : (N <= 4096 ? 1 : 0);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tau = cfg.tau;
   cudaEvent_t ea = nullptr, eb = nullptr;

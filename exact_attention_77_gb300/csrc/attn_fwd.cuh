@@ -73,7 +73,9 @@ struct FwdLayout {
   static constexpr int kBarSFull = kBarKVEmpty + kStages;
   static constexpr int kBarPFull = kBarSFull + NQT;
   static constexpr int kBarODone = kBarPFull + NQT;
-  static constexpr int kBarMmaDone = kBarODone + NQT;
+  static constexpr int kBarOFree = kBarODone + NQT;    // + t: O_t read out by the epilogue (128 arrivals)
+  static constexpr int kBarQEmpty = kBarOFree + NQT;   // the unit's last S products have read Q
+  static constexpr int kBarMmaDone = kBarQEmpty + 1;
   static constexpr int kNumBars = kBarMmaDone + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   // Tensor memory decides residency: two CTAs of 256 columns per SM, or one of
@@ -87,11 +89,11 @@ struct FwdLayout {
 
 // Where-codes recorded with a timeout (role * 10 + wait).
 enum : int {
-  kWhereProdEmpty = 10, kWhereMmaQ = 20, kWhereMmaKV = 21, kWhereMmaP = 22,
+  kWhereProdEmpty = 10, kWhereMmaQ = 20, kWhereMmaKV = 21, kWhereMmaP = 22, kWhereMmaO = 23,
   kWhereSmS = 30, kWhereSmO = 31, kWhereSmFinal = 32, kWhereAlign = 1
 };
 
-template <int DQK, int DV, int NQT, bool CAUSAL, int POLY>
+template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool PERSIST>
 __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<DQK, DV, NQT>::kMinBlocks)
     fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<DQK, DV, NQT>;
@@ -108,28 +110,48 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
-  // ---- work unit: (bh, block of NQT query tiles)
+  // ---- work units: (bh, block of NQT query tiles).  The CTA is persistent:
+  // it takes units blockIdx.x, blockIdx.x + gridDim.x, ... and every role
+  // runs its pipeline straight across unit boundaries (barrier phases and
+  // the K/V ring position carry over), so the next unit's Q, K and V load
+  // and its first products issue while this unit's epilogue runs.
   const int n_qblocks = (p.n_qtiles + NQT - 1) / NQT;
-  int bh, qblock;
-  if (CAUSAL) {  // longest rows first, spread over heads
-    const int rank = blockIdx.x / p.BH;
-    bh = blockIdx.x - rank * p.BH;
-    qblock = n_qblocks - 1 - rank;
-  } else {  // head-major keeps one head's K/V hot in L2
-    bh = blockIdx.x / n_qblocks;
-    qblock = blockIdx.x - bh * n_qblocks;
-  }
-  int nkv[NQT];
-  int nkv_max = 0;
+  struct Unit {
+    int bh, qblock, nkv[NQT], nkv_max;
+  };
+  auto unit_at = [&](int u) {
+    Unit w;
+    if (CAUSAL) {  // longest rows first, spread over heads
+      const int rank = u / p.BH;
+      w.bh = u - rank * p.BH;
+      w.qblock = n_qblocks - 1 - rank;
+    } else {  // head-major keeps one head's K/V hot in L2
+      w.bh = u / n_qblocks;
+      w.qblock = u - w.bh * n_qblocks;
+    }
+    w.nkv_max = 0;
 #pragma unroll
-  for (int t = 0; t < NQT; ++t) {
-    const int qt = qblock * NQT + t;
-    nkv[t] = qt < p.n_qtiles ? (CAUSAL ? qt + 1 : p.n_qtiles) : 0;
-    nkv_max = nkv[t] > nkv_max ? nkv[t] : nkv_max;
-  }
+    for (int t = 0; t < NQT; ++t) {
+      const int qt = w.qblock * NQT + t;
+      w.nkv[t] = qt < p.n_qtiles ? (CAUSAL ? qt + 1 : p.n_qtiles) : 0;
+      w.nkv_max = w.nkv[t] > w.nkv_max ? w.nkv[t] : w.nkv_max;
+    }
+    return w;
+  };
+  // CTA b takes, in round r, unit r*G + b (r even) or r*G + G-1-b (r odd):
+  // with the units sorted longest first (causal), the serpentine order hands
+  // every CTA a similar total.
+  // Without PERSIST the grid has one CTA per unit and all of this folds away.
+  const int n_units = PERSIST ? p.n_blocks : (int)gridDim.x;
+  const int G = gridDim.x;
+  const int n_rounds = PERSIST ? (n_units + G - 1) / G : 1;
+  auto unit_of_round = [&](int r) {
+    return PERSIST ? r * G + ((r & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x) : (int)blockIdx.x;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kBarQFull), 1);
+    mbar_init(bar(L::kBarQEmpty), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarKVFull + s), 1);
       mbar_init(bar(L::kBarKVEmpty + s), 1);
@@ -138,6 +160,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       mbar_init(bar(L::kBarSFull + t), 1);
       mbar_init(bar(L::kBarPFull + t), 128);
       mbar_init(bar(L::kBarODone + t), 1);
+      mbar_init(bar(L::kBarOFree + t), 128);
     }
     mbar_init(bar(L::kBarMmaDone), 1);
     *abort_flag = 0;
@@ -160,42 +183,50 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       prefetch_tensormap(&p.tm_q);
       prefetch_tensormap(&p.tm_k);
       prefetch_tensormap(&p.tm_v);
-      mbar_arrive_expect_tx(bar(L::kBarQFull), NQT * L::kQBytes);
-#pragma unroll
-      for (int t = 0; t < NQT; ++t)
-#pragma unroll
-        for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sbase + t * L::kQBytes + c * kSubTile, &p.tm_q, c * 64, (qblock * NQT + t) * kTile, bh,
-                      bar(L::kBarQFull));
-      int issued = 0;
+      int issued = 0;  // K/V loads so far (K_j and V_j alternate through the ring)
+      int qn = 0;      // units started
       bool ok = true;
-      for (int j = 0; ok && j < nkv_max; ++j) {
+      for (int r = 0; ok && r < n_rounds; ++r) {
+        const int u = unit_of_round(r);
+        if (u >= n_units) continue;
+        const Unit w = unit_at(u);
+        if (PERSIST && qn > 0 && !mbar_wait(bar(L::kBarQEmpty), (qn - 1) & 1, ctl, kWhereProdEmpty)) break;
+        mbar_arrive_expect_tx(bar(L::kBarQFull), NQT * L::kQBytes);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int ld = 2 * j + h;
-          const int s = ld % L::kStages;
-          if (!mbar_wait(bar(L::kBarKVEmpty + s), ((ld / L::kStages) & 1) ^ 1, ctl, kWhereProdEmpty)) {
-            ok = false;
-            break;
+        for (int t = 0; t < NQT; ++t)
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c)
+            tma_load_3d(sbase + t * L::kQBytes + c * kSubTile, &p.tm_q, c * 64, (w.qblock * NQT + t) * kTile, w.bh,
+                        bar(L::kBarQFull));
+        ++qn;
+        for (int j = 0; ok && j < w.nkv_max; ++j) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int ld = issued;
+            const int s = ld % L::kStages;
+            if (!mbar_wait(bar(L::kBarKVEmpty + s), ((ld / L::kStages) & 1) ^ 1, ctl, kWhereProdEmpty)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = sbase + L::kKVOff + s * L::kStageBytes;
+            ATTN_TRACE_AT(blockIdx.x, j, 13 + h);
+            if (h == 0) {
+              mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
+#pragma unroll
+              for (int c = 0; c < DQK / 64; ++c)
+                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * 64, j * kTile, w.bh, bar(L::kBarKVFull + s));
+            } else {
+              mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kVBytes);
+#pragma unroll
+              for (int c = 0; c < DV / 64; ++c)
+                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * 64, j * kTile, w.bh, bar(L::kBarKVFull + s));
+            }
+            issued = ld + 1;
           }
-          const uint32_t dst = sbase + L::kKVOff + s * L::kStageBytes;
-          ATTN_TRACE_AT(blockIdx.x, j, 13 + h);
-          if (h == 0) {
-            mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
-#pragma unroll
-            for (int c = 0; c < DQK / 64; ++c)
-              tma_load_3d(dst + c * kSubTile, &p.tm_k, c * 64, j * kTile, bh, bar(L::kBarKVFull + s));
-          } else {
-            mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kVBytes);
-#pragma unroll
-            for (int c = 0; c < DV / 64; ++c)
-              tma_load_3d(dst + c * kSubTile, &p.tm_v, c * 64, j * kTile, bh, bar(L::kBarKVFull + s));
-          }
-          issued = ld + 1;
         }
       }
       // copies still in flight must land before the CTA can exit
-      mbar_wait_drain(bar(L::kBarQFull), 0, p.timeout_ns);
+      if (qn > 0) mbar_wait_drain(bar(L::kBarQFull), (qn - 1) & 1, p.timeout_ns);
       for (int ld = issued > L::kStages ? issued - L::kStages : 0; ld < issued; ++ld)
         mbar_wait_drain(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1, p.timeout_ns);
     }
@@ -230,51 +261,88 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
         mma_ts_elect(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * 2048), kIdescPV,
                      (acc || kk > 0) ? 1u : 0u);
     };
-    bool ok = wait_all(bar(L::kBarQFull), 0, kWhereMmaQ);
-    if (ok && nkv_max > 0) {
-      ok = wait_load(0);
-      if (ok) {
+    bool ok = true;
+    int ld0 = 0;  // ring position of this unit's K_0
+    int qn = 0;   // units started
+    // parity of the P-ready phases consumed so far per tile, and whether the
+    // tile's O columns still hold an output the epilogue has not read
+    uint32_t pbit[NQT], obit[NQT];
+    bool owed[NQT];
+#pragma unroll
+    for (int t = 0; t < NQT; ++t) {
+      pbit[t] = obit[t] = 0;
+      owed[t] = false;
+    }
+    for (int r = 0; ok && r < n_rounds; ++r) {
+      const int u = unit_of_round(r);
+      if (u >= n_units) continue;
+      const Unit w = unit_at(u);
+      if (!(ok = wait_all(bar(L::kBarQFull), qn & 1, kWhereMmaQ))) break;
+      ++qn;
+      if (w.nkv_max > 0) {
+        if (!(ok = wait_load(ld0))) break;
 #pragma unroll
         for (int t = 0; t < NQT; ++t)
-          if (nkv[t] > 0) {
-            issue_qk(t, 0);
+          if (w.nkv[t] > 0) {
+            issue_qk(t, ld0 % L::kStages);
             tc_commit_elect(bar(L::kBarSFull + t));
           }
-        tc_commit_elect(bar(L::kBarKVEmpty + 0));
+        tc_commit_elect(bar(L::kBarKVEmpty + ld0 % L::kStages));
       }
-    }
-    for (int j = 0; ok && j < nkv_max; ++j) {
-      const int ldv = 2 * j + 1;
-      const int ldk = 2 * j + 2;
-      if (!(ok = wait_load(ldv))) break;
-      if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 0);
-      bool k_ready = false;
+      // O_t is overwritten by this unit's first P V product: the previous
+      // unit's epilogue must have read it out
 #pragma unroll
-      for (int t = 0; t < NQT; ++t) {
-        if (ok && j < nkv[t]) {
-          ok = wait_all(bar(L::kBarPFull + t), j & 1, kWhereMmaP);
-          if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 1 + 4 * t);
-          if (ok) {
-            issue_pv(t, ldv % L::kStages, j > 0);
-            tc_commit_elect(bar(L::kBarODone + t));
-            if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 2 + 4 * t);
+      for (int t = 0; t < NQT; ++t)
+        if (PERSIST && ok && owed[t] && w.nkv[t] > 0) {
+          ok = wait_all(bar(L::kBarOFree + t), obit[t], kWhereMmaO);
+          obit[t] ^= 1;
+          owed[t] = false;
+        }
+      if (!ok) break;
+      // the steady-state loop (as for a single unit; ring positions and
+      // phases offset by this unit's start)
+      for (int j = 0; ok && j < w.nkv_max; ++j) {
+        const int ldv = ld0 + 2 * j + 1;
+        const int ldk = ldv + 1;
+        if (!(ok = wait_load(ldv))) break;
+        if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 0);
+        bool k_ready = false;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (ok && j < w.nkv[t]) {
+            ok = wait_all(bar(L::kBarPFull + t), pbit[t] ^ (j & 1), kWhereMmaP);
+            if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 1 + 4 * t);
+            if (ok) {
+              issue_pv(t, ldv % L::kStages, j > 0);
+              tc_commit_elect(bar(L::kBarODone + t));
+              if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 2 + 4 * t);
+            }
+          }
+          if (ok && j + 1 < w.nkv[t]) {
+            if (!k_ready) {
+              ok = k_ready = wait_load(ldk);
+              if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 3);
+            }
+            if (ok) {
+              issue_qk(t, ldk % L::kStages);
+              tc_commit_elect(bar(L::kBarSFull + t));
+              if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 4 + 4 * t);
+            }
           }
         }
-        if (ok && j + 1 < nkv[t]) {
-          if (!k_ready) {
-            ok = k_ready = wait_load(ldk);
-            if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 3);
-          }
-          if (ok) {
-            issue_qk(t, ldk % L::kStages);
-            tc_commit_elect(bar(L::kBarSFull + t));
-            if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 4 + 4 * t);
-          }
-        }
+        if (!ok) break;
+        tc_commit_elect(bar(L::kBarKVEmpty + ldv % L::kStages));
+        if (k_ready) tc_commit_elect(bar(L::kBarKVEmpty + ldk % L::kStages));
       }
       if (!ok) break;
-      tc_commit_elect(bar(L::kBarKVEmpty + ldv % L::kStages));
-      if (k_ready) tc_commit_elect(bar(L::kBarKVEmpty + ldk % L::kStages));
+      if (PERSIST) tc_commit_elect(bar(L::kBarQEmpty));  // Q may be reloaded for the next unit
+#pragma unroll
+      for (int t = 0; t < NQT; ++t)
+        if (w.nkv[t] > 0) {
+          pbit[t] ^= (uint32_t)(w.nkv[t] & 1);
+          owed[t] = true;
+        }
+      ld0 += 2 * w.nkv_max;
     }
     // every product issued above completes before tensor memory is freed
     tc_commit_elect(bar(L::kBarMmaDone));
@@ -284,20 +352,21 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
 #ifdef ATTN_TRACE
    else if (warp == 2) {
     // debug only: completion times of the product groups, seen by polling
-    if (lane == 0 && blockIdx.x < kTraceCtas) {
+    if (lane == 0 && blockIdx.x < kTraceCtas && u0 < n_units) {
+      const Unit w0 = unit_at(u0);  // the first unit only
       bool live = true;
       auto seen = [&](uint32_t b, uint32_t par) {
         for (int i = 0; live && i < (1 << 22); ++i)
           if (mbar_test(b, par)) return;
         live = false;
       };
-      for (int j = 0; live && j < nkv_max && j < kTraceIters; ++j)
+      for (int j = 0; live && j < w0.nkv_max && j < kTraceIters; ++j)
         for (int t = 0; t < NQT; ++t) {
-          if (j < nkv[t]) {
+          if (j < w0.nkv[t]) {
             seen(bar(L::kBarODone + t), j & 1);
             ATTN_TRACE_AT(blockIdx.x, j, 16 + 2 * t);
           }
-          if (j + 1 < nkv[t]) {
+          if (j + 1 < w0.nkv[t]) {
             seen(bar(L::kBarSFull + t), (j + 1) & 1);
             ATTN_TRACE_AT(blockIdx.x, j, 17 + 2 * t);
           }
@@ -306,9 +375,10 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     __syncwarp();
    } else if (warp == 3) {
     // debug only: landing times of the K_j / V_j tiles
-    if (lane == 0 && blockIdx.x < kTraceCtas) {
+    if (lane == 0 && blockIdx.x < kTraceCtas && u0 < n_units) {
+      const Unit w0 = unit_at(u0);  // the first unit only
       bool live = true;
-      for (int ld = 0; live && ld < 2 * nkv_max && ld / 2 < kTraceIters; ++ld) {
+      for (int ld = 0; live && ld < 2 * w0.nkv_max && ld / 2 < kTraceIters; ++ld) {
         int i = 0;
         for (; i < (1 << 22); ++i)
           if (mbar_test(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1)) break;
@@ -324,18 +394,25 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     // ====================== softmax warpgroups =======================
     const int t = (warp - 4) >> 2;
     const int quad = warp & 3;  // this warp may touch tensor-memory lanes 32*quad .. 32*quad+31
-    const int qt = qblock * NQT + t;
-    const int q_row = qt * kTile + quad * 32 + lane;
     const uint32_t tS = tmem + ((uint32_t)(quad * 32) << 16) + t * 256;
     const uint32_t tO = tS + 128;
-    const int n = nkv[t];
     const float c_log2 = p.scale_log2;
-    float m = -INFINITY;  // running (possibly stale) max, log2 units
-    float l = 0.f;        // running sum of 2^(s*c - m)
     unsigned rescales = 0;
     bool ok = true;
+    uint32_t cbit = 0;  // parity of the S / P / O-done phases of this tile in earlier units
+    for (int r = 0; ok && r < n_rounds; ++r) {
+    const int u = unit_of_round(r);
+    if (u >= n_units) continue;
+    const Unit w = unit_at(u);
+    const int n = w.nkv[t];
+    if (n == 0) continue;
+    const int bh = w.bh;
+    const int qt = w.qblock * NQT + t;
+    const int q_row = qt * kTile + quad * 32 + lane;
+    float m = -INFINITY;  // running (possibly stale) max, log2 units
+    float l = 0.f;        // running sum of 2^(s*c - m)
     for (int j = 0; j < n; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), j & 1, ctl, kWhereSmS));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), cbit ^ (j & 1), ctl, kWhereSmS));
       if (!ok) break;
       if (quad == 0 && lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 9 + 2 * t);
       tc_fence_after();
@@ -372,7 +449,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
         rescales += (j > 0 && need) ? 1u : 0u;
         l *= alpha;
         if (j > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), (j - 1) & 1, ctl, kWhereSmO));
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), cbit ^ ((j - 1) & 1), ctl, kWhereSmO));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -411,8 +488,8 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       mbar_arrive(bar(L::kBarPFull + t));
       if (quad == 0 && lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 10 + 2 * t);
     }
-    if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), (n - 1) & 1, ctl, kWhereSmFinal));
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), cbit ^ ((n - 1) & 1), ctl, kWhereSmFinal));
       if (ok) {
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -432,9 +509,16 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
               orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
         }
+        // O_t has been read out: the next unit's products may overwrite it
+        if (PERSIST) {
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarOFree + t));
+        }
         if (live) p.lse[(size_t)bh * p.N + q_row] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
+    cbit ^= (uint32_t)(n & 1);
+    }  // units
     if (p.rescale_counter != nullptr) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) rescales += __shfl_xor_sync(0xffffffffu, rescales, off);
@@ -453,7 +537,11 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
 template <int DQK, int DV, int NQT, bool CAUSAL, int POLY>
 cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<DQK, DV, NQT>;
-  auto kernel = fwd_kernel<DQK, DV, NQT, CAUSAL, POLY>;
+  // Persistent CTAs pay off when units are short (few K/V tiles each); with
+  // long units the one-unit-per-CTA kernel is leaner and the launch order
+  // already balances.  p.max_ctas > 0 forces the persistent grid.
+  const bool persist = p.max_ctas > 0 || p.persist;
+  auto kernel = persist ? fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, true> : fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits until the registers it asks for are free, so the
@@ -462,7 +550,17 @@ cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != L::kLaunchRegs) return cudaErrorInvalidConfiguration;
-  kernel<<<p.n_blocks, L::kThreads, L::kSmemBytes, stream>>>(p);
+  // persistent grid: as many CTAs as fit on the device at once, each looping
+  // over work units (p.max_ctas > 0 sets the grid instead, e.g. one unit per
+  // CTA when it is at least the number of units)
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  int grid = !persist ? p.n_blocks : p.max_ctas > 0 ? p.max_ctas : sms * L::kMinBlocks;
+  if (grid > p.n_blocks) grid = p.n_blocks;
+  kernel<<<grid, L::kThreads, L::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

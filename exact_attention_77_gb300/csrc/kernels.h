@@ -23,6 +23,8 @@ struct FwdParams {
   int BH;
   int n_qtiles;  // ceil(N / 128)
   int n_blocks;  // work units: BH * ceil(n_qtiles / tiles per CTA)
+  int max_ctas;  // persistent grid size (0: as many CTAs as fit)
+  int persist;   // 1: persistent CTAs looping over units; 0: one CTA per unit
   float scale_log2;  // scale * log2(e)
   float tau;         // rescale threshold, log2 units
 };
