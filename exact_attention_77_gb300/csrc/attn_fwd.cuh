@@ -288,6 +288,9 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
             tc_commit_elect(bar(L::kBarSFull + t));
           }
         tc_commit_elect(bar(L::kBarKVEmpty + ld0 % L::kStages));
+        // Q may be reloaded for the next unit once this unit's last S
+        // products complete (here, or inside the loop below)
+        if (PERSIST && w.nkv_max == 1) tc_commit_elect(bar(L::kBarQEmpty));
       }
       // O_t is overwritten by this unit's first P V product: the previous
       // unit's epilogue must have read it out
@@ -331,11 +334,12 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
           }
         }
         if (!ok) break;
+        if (PERSIST && j + 2 == w.nkv_max) tc_commit_elect(bar(L::kBarQEmpty));
         tc_commit_elect(bar(L::kBarKVEmpty + ldv % L::kStages));
         if (k_ready) tc_commit_elect(bar(L::kBarKVEmpty + ldk % L::kStages));
       }
       if (!ok) break;
-      if (PERSIST) tc_commit_elect(bar(L::kBarQEmpty));  // Q may be reloaded for the next unit
+      if (PERSIST && w.nkv_max == 0) tc_commit_elect(bar(L::kBarQEmpty));
 #pragma unroll
       for (int t = 0; t < NQT; ++t)
         if (w.nkv[t] > 0) {
