@@ -38,6 +38,7 @@ _SIGS = {
     "attn_exp2_throughput": (_I, [_P, _I, _I, _I, _P]),
     "attn_set_rescale_counter": (_I, [_P]),
     "attn_set_rescale_threshold": (_I, [_F]),
+    "attn_set_bwd_pair": (_I, [_I]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_profile_start": (_I, []),
@@ -167,6 +168,10 @@ def attn_set_rescale_counter(counter):
 
 def attn_set_rescale_threshold(tau: float):
     _check(get_lib().attn_set_rescale_threshold(float(tau)))
+
+
+def attn_set_bwd_pair(enable: int):
+    _check(get_lib().attn_set_bwd_pair(int(enable)))
 
 
 def attn_selftest_wait_timeout(timeout_us: int, stream=None):

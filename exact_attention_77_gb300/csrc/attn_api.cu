@@ -27,6 +27,7 @@ struct Settings {
   int fwd_poly = 0;   // 1: a share of the exponentials on the FMA-pipe polynomial
   int fwd_max_ctas = 0;  // persistent forward grid size (0: one CTA per free SM slot)
   int fwd_persist = -1;  // -1: by sequence length; 0 / 1 forces
+  int bwd_pair = 0;      // 1: d = 128 backward on CTA pairs
   float tau = 8.0f;
   unsigned long long* rescale_counter = nullptr;
 };
@@ -74,6 +75,7 @@ Settings settings() {
     if (const char* e = getenv("ATTN_EXP_POLY")) g_settings.fwd_poly = atoi(e) != 0;
     if (const char* e = getenv("ATTN_FWD_MAX_CTAS")) g_settings.fwd_max_ctas = atoi(e);
     if (const char* e = getenv("ATTN_FWD_PERSIST")) g_settings.fwd_persist = atoi(e);
+    if (const char* e = getenv("ATTN_BWD_PAIR")) g_settings.bwd_pair = atoi(e) != 0;
   }
   return g_settings;
 }
@@ -109,12 +111,12 @@ int encoder(EncodeTiledFn* out) {
 
 // 3-D view [BH, N, d] of a contiguous bf16 tensor; box 64 (d) x 128 (rows) x 1
 // with the 128-byte swizzle; rows past N read as zero.
-int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128) {
   EncodeTiledFn enc;
   if (int st = encoder(&enc)) return st;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -179,6 +181,14 @@ int attn_set_rescale_counter(unsigned long long* counter) {
   settings();
   std::lock_guard<std::mutex> lock(g_mu);
   g_settings.rescale_counter = counter;
+  return ATTN_OK;
+}
+
+int attn_set_bwd_pair(int enable) {
+  if (enable != 0 && enable != 1) return ATTN_ERR_INVALID_ARG;
+  settings();
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_settings.bwd_pair = enable;
   return ATTN_OK;
 }
 
@@ -261,6 +271,12 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (int st = make_map(&p.tm_k, k, BH, N, d_qk)) return st;
   if (int st = make_map(&p.tm_v, v, BH, N, d_v)) return st;
   if (int st = make_map(&p.tm_do, dO, BH, N, d_v)) return st;
+  // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)
+  p.pair_mode = (d_qk == 128 && cfg.bwd_pair) ? 1 : 0;
+  if (p.pair_mode) {
+    if (int st = make_map(&p.tm_q_half, q, BH, N, d_qk, 64)) return st;
+    if (int st = make_map(&p.tm_do_half, dO, BH, N, d_v, 64)) return st;
+  }
   if (int st = status_ptr(&p.status)) return st;
   char* ws = static_cast<char*>(workspace);
   p.o = o;

@@ -184,8 +184,10 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(BwdParams p) {
   const int bh = (int)(row / p.N);
   const int i = (int)(row - (long)bh * p.N);
   const int tile = i >> 7, r = i & 127;
-  const float4 a = *reinterpret_cast<const float4*>(
-      p.dq_acc + ((((size_t)bh * p.n_tiles + tile) * kGroups + g) * 128 + r) * 4);
+  // pair mode: each tile's accumulator is two [D/4][64][4] row halves
+  const size_t idx = p.pair_mode ? ((((size_t)bh * p.n_tiles + tile) * 2 + (r >> 6)) * kGroups + g) * 64 + (r & 63)
+                                 : (((size_t)bh * p.n_tiles + tile) * kGroups + g) * 128 + r;
+  const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + idx * 4);
   uint2 out;
   out.x = pack_bf16(a.x * p.scale, a.y * p.scale);
   out.y = pack_bf16(a.z * p.scale, a.w * p.scale);
@@ -644,6 +646,10 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
   }
 }
 
+// Main kernel of the CTA-pair backward (defined in attn_bwd2.cuh, d = 128).
+template <bool CAUSAL, bool DET>
+cudaError_t launch_bwd2_main(const BwdParams& p, cudaStream_t stream);
+
 template <int D, bool CAUSAL, bool DET>
 cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const LaunchEvents* evs) {
   using L = BwdLayout<D>;
@@ -661,7 +667,15 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
     if (e != cudaSuccess) return e;
   }
   mark(1);
-  {
+  bool paired = false;
+  if constexpr (D == 128) {
+    if (p.pair_mode) {
+      cudaError_t e = launch_bwd2_main<CAUSAL, DET>(p, stream);
+      if (e != cudaSuccess) return e;
+      paired = true;
+    }
+  }
+  if (!paired) {
     auto kernel = bwd_kernel<D, CAUSAL, DET>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -1,7 +1,22 @@
 // Backward kernel instances for d_qk = d_v = 128.
-#include "attn_bwd.cuh"
+#include "attn_bwd2.cuh"
 
 namespace attn {
+
+template <bool CAUSAL, bool DET>
+cudaError_t launch_bwd2_main(const BwdParams& p, cudaStream_t stream) {
+  using L = Bwd2Layout;
+  auto kernel = bwd2_kernel<CAUSAL, DET>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != L::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  const int n_pairs = (p.n_tiles + 1) / 2;
+  kernel<<<p.BH * n_pairs * 2, L::kThreads, L::kSmemBytes, stream>>>(p);  // clusters of two (kernel attribute)
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s, const LaunchEvents* ev) {
   if (causal) return deterministic ? launch_bwd_instance<128, true, true>(p, s, ev) : launch_bwd_instance<128, true, false>(p, s, ev);

@@ -356,8 +356,8 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
 #ifdef ATTN_TRACE
    else if (warp == 2) {
     // debug only: completion times of the product groups, seen by polling
-    if (lane == 0 && blockIdx.x < kTraceCtas && u0 < n_units) {
-      const Unit w0 = unit_at(u0);  // the first unit only
+    if (lane == 0 && blockIdx.x < kTraceCtas && unit_of_round(0) < n_units) {
+      const Unit w0 = unit_at(unit_of_round(0));  // the first unit only
       bool live = true;
       auto seen = [&](uint32_t b, uint32_t par) {
         for (int i = 0; live && i < (1 << 22); ++i)
@@ -379,8 +379,8 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     __syncwarp();
    } else if (warp == 3) {
     // debug only: landing times of the K_j / V_j tiles
-    if (lane == 0 && blockIdx.x < kTraceCtas && u0 < n_units) {
-      const Unit w0 = unit_at(u0);  // the first unit only
+    if (lane == 0 && blockIdx.x < kTraceCtas && unit_of_round(0) < n_units) {
+      const Unit w0 = unit_at(unit_of_round(0));  // the first unit only
       bool live = true;
       for (int ld = 0; live && ld < 2 * w0.nkv_max && ld / 2 < kTraceIters; ++ld) {
         int i = 0;

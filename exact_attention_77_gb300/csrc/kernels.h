@@ -34,6 +34,8 @@ struct BwdParams {
   CUtensorMap tm_k;   // [BH, N, d_qk]
   CUtensorMap tm_v;   // [BH, N, d_v]
   CUtensorMap tm_do;  // [BH, N, d_v]
+  CUtensorMap tm_q_half;   // Q with 64-row boxes (CTA-pair backward)
+  CUtensorMap tm_do_half;  // dO with 64-row boxes (CTA-pair backward)
   const void* o;      // bf16 [BH, N, d_v]
   const void* dO;     // bf16 [BH, N, d_v]
   const float* lse;   // fp32 [BH, N]
@@ -42,7 +44,7 @@ struct BwdParams {
   void* dv;           // bf16 [BH, N, d_v]
   float* row_lse2;    // workspace fp32 [BH, Npad]: -LSE * log2(e), -inf on padding rows
   float* row_d;       // workspace fp32 [BH, Npad]: -rowsum(dO * O), 0 on padding rows
-  float* dq_acc;      // workspace fp32 [BH, n_tiles, d_qk/4, 128, 4]
+  float* dq_acc;      // workspace fp32 [BH, n_tiles, d_qk/4, 128, 4]; [BH, n_tiles, 2, d_qk/4, 64, 4] when pair_mode
   int* tickets;       // workspace int32 [BH, n_tiles] (deterministic mode)
   DeviceStatus* status;
   unsigned long long timeout_ns;
@@ -52,6 +54,7 @@ struct BwdParams {
   int n_tiles;   // ceil(N / 128)
   float scale;
   float scale_log2;
+  int pair_mode;  // 1: CTA-pair main kernel (d = 128) and its accumulator layout
 };
 
 // Optional events recorded on the launch stream around each backward kernel:

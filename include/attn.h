@@ -146,6 +146,23 @@ int attn_set_rescale_counter(unsigned long long* counter);
 int attn_set_rescale_threshold(float tau);
 
 /*
+ * Backward on CTA pairs at d = 128 ("FlashAttention-4: Algorithm and Kernel
+ * Pipelining Co-Design for Asymmetric Hardware Scaling", Table 3 and Figure
+ * 3: the 2-CTA backward).  With enable = 1, later attn_bwd calls with
+ * d_qk = d_v = 128 run the main kernel on clusters of two CTAs: key tiles
+ * 2p and 2p+1 of a head share every product (tcgen05.mma.cta_group::2,
+ * M = 256, each CTA reading half of the B operand), and dQ of a query tile is
+ * one pair product over both key tiles after the CTAs exchange dS halves
+ * through distributed shared memory.  Results meet the same tolerances and
+ * the deterministic mode stays bit-reproducible; the accumulator layout in
+ * the workspace differs (workspace size unchanged).  enable = 0 (the
+ * default; also the environment variable ATTN_BWD_PAIR=0/1 at first use)
+ * selects the one-CTA kernel, which measures faster on GB300.  Returns
+ * ATTN_OK or ATTN_ERR_INVALID_ARG (enable not 0 or 1).
+ */
+int attn_set_bwd_pair(int enable);
+
+/*
  * Per-kernel timing for benchmarks.  Between attn_profile_start and
  * attn_profile_stop, every attn_fwd / attn_bwd call on any stream also records
  * CUDA events immediately before and after each of its kernel launches, on

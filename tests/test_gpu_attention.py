@@ -211,3 +211,58 @@ def test_config5_backward_sweep(A, N, causal):
         for name, got, ref in zip(("dq", "dk", "dv"), grads, refs):
             e = G.rel_fro(G.f64(got[b, h]), ref)
             assert e <= G.GRAD_REL, (name, det, e)
+
+
+# ------------------------------------ CTA-pair backward (d = 128, opt-in)
+@pytest.fixture
+def pair_mode(A):
+    A.attn_set_bwd_pair(1)
+    yield
+    A.attn_set_bwd_pair(0)
+
+
+@pytest.mark.parametrize("N", [1, 100, 128, 257, 384, 640])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("det", [0, 1])
+def test_backward_pair_ragged_and_small(A, pair_mode, N, causal, det):
+    """Key-tile pairs, including a ragged last pair whose odd CTA has no keys."""
+    B, H, d = 1, 2, 128
+    t = G.inputs(B, H, N, d, d, seed=13)
+    o, lse = G.run_fwd(A, t, causal)
+    dq, dk, dv = G.run_bwd(A, t, o, lse, causal, det)
+    G.check_status(A)
+    q, k, v, do = (G.f64(t[n]) for n in ("q", "k", "v", "do"))
+    refs = ora.backward(q, k, v, do, 1.0 / math.sqrt(d), bool(causal))
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        G.assert_grad_close(name, G.f64(got), ref)
+
+
+@pytest.mark.parametrize("N", [4096, 16384])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_backward_pair_config5(A, pair_mode, N, causal):
+    """d=128, H=16, B*N=16384, both dQ modes on CTA pairs: one seeded full head."""
+    B, H, d = 16384 // N, 16, 128
+    t = G.inputs(B, H, N, d, d)
+    o, lse = G.run_fwd(A, t, causal)
+    rng = np.random.Generator(np.random.PCG64(70 + N + causal))
+    b, h = int(rng.integers(B)), int(rng.integers(H))
+    q, k, v, do = (G.f64(t[n][b, h]) for n in ("q", "k", "v", "do"))
+    refs = ora.backward_head(q, k, v, do, 1.0 / math.sqrt(d), bool(causal))
+    for det in (0, 1):
+        grads = G.run_bwd(A, t, o, lse, causal, det)
+        G.check_status(A)
+        for name, got, ref in zip(("dq", "dk", "dv"), grads, refs):
+            e = G.rel_fro(G.f64(got[b, h]), ref)
+            assert e <= G.GRAD_REL, (name, det, e)
+
+
+def test_backward_pair_deterministic_is_bit_identical(A, pair_mode):
+    torch = G.torch_mod()
+    t = G.inputs(2, 4, 1024, 128, 128, seed=5)
+    for causal in (0, 1):
+        o, lse = G.run_fwd(A, t, causal)
+        runs = [G.run_bwd(A, t, o, lse, causal, 1) for _ in range(3)]
+        G.check_status(A)
+        for r in runs[1:]:
+            for a, b in zip(runs[0], r):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
