@@ -14,6 +14,8 @@ attention   the plain definition of scaled-dot-product attention (two-pass
 exp2_poly   the 2^x polynomial emulation: our own minimax fit and its error
             table.
 roofline    the cycle model behind the forward and backward roofline tables.
+merge       attention over a key range (split-KV partials) and the associative
+            merge of such partials.
 
 Every function is pinned by a CPU test against something other than itself
 (brute force, finite differences, closed forms, invariants, or the numbers
