@@ -41,6 +41,10 @@ _SIGS = {
     "attn_set_bwd_pair": (_I, [_I]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t, _P]),
+    "attn_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "attn_splitkv_heuristic": (_I, [_I, _I, _I, _I, _I, _I]),
+    "attn_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _P]),
     "attn_profile_start": (_I, []),
     "attn_profile_stop": (_I, [_P]),
 }
@@ -49,7 +53,8 @@ _SIGS = {
 class attn_kernel_times_t(ctypes.Structure):
     _fields_ = [("launches_fwd", _I), ("launches_bwd_pre", _I), ("launches_bwd_main", _I),
                 ("launches_bwd_convert", _I), ("ms_fwd", _F), ("ms_bwd_pre", _F), ("ms_bwd_main", _F),
-                ("ms_bwd_convert", _F)]
+                ("ms_bwd_convert", _F), ("launches_fwd_split", _I), ("launches_merge", _I), ("ms_fwd_split", _F),
+                ("ms_merge", _F)]
 
 
 class AttnError(RuntimeError):
@@ -128,6 +133,32 @@ def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, causal, scale,
     st = get_lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N,
                       d_qk, d_v, int(causal), float(scale), int(deterministic), _ptr(workspace), int(workspace_bytes),
                       _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, B, H, N_q, N_k, d_qk, d_v, scale, n_splits, workspace, workspace_bytes,
+                     stream=None, check=True) -> int:
+    st = get_lib().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N_q, N_k, d_qk, d_v,
+                                    float(scale), int(n_splits), _ptr(workspace), int(workspace_bytes),
+                                    _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_fwd_splitkv_workspace_bytes(B, H, N_q, N_k, d_v, n_splits) -> int:
+    return get_lib().attn_fwd_splitkv_workspace_bytes(B, H, N_q, N_k, d_v, int(n_splits))
+
+
+def attn_splitkv_heuristic(B, H, N_q, N_k, d_qk, n_sms) -> int:
+    return get_lib().attn_splitkv_heuristic(B, H, N_q, N_k, d_qk, int(n_sms))
+
+
+def attn_merge(o_parts, lse_parts, n_parts, o, lse, BH, N, d_v, stream=None, check=True) -> int:
+    st = get_lib().attn_merge(_ptr(o_parts), _ptr(lse_parts), int(n_parts), _ptr(o), _ptr(lse), BH, N, d_v,
+                              _stream(stream))
     if check:
         _check(st)
     return st

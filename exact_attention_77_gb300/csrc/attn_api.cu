@@ -28,6 +28,7 @@ struct Settings {
   int fwd_max_ctas = 0;  // persistent forward grid size (0: one CTA per free SM slot)
   int fwd_persist = -1;  // -1: by sequence length; 0 / 1 forces
   int bwd_pair = 0;      // 1: d = 128 backward on CTA pairs
+  int merge_pdl = 1;     // 1: split-KV merge as a programmatic dependent launch
   float tau = 8.0f;
   unsigned long long* rescale_counter = nullptr;
 };
@@ -42,7 +43,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-// Events recorded while profiling: kind 0 = forward, 1..3 = backward pieces.
+// Events recorded while profiling: kind 0 = forward, 1..3 = backward pieces,
+// 4 / 5 = split-KV forward / merge.
 struct ProfileRecord {
   int kind;
   cudaEvent_t a, b;
@@ -76,6 +78,7 @@ Settings settings() {
     if (const char* e = getenv("ATTN_FWD_MAX_CTAS")) g_settings.fwd_max_ctas = atoi(e);
     if (const char* e = getenv("ATTN_FWD_PERSIST")) g_settings.fwd_persist = atoi(e);
     if (const char* e = getenv("ATTN_BWD_PAIR")) g_settings.bwd_pair = atoi(e) != 0;
+    if (const char* e = getenv("ATTN_MERGE_PDL")) g_settings.merge_pdl = atoi(e) != 0;
   }
   return g_settings;
 }
@@ -159,7 +162,85 @@ WorkspaceLayout workspace_layout(int B, int H, int N, int d_qk, int deterministi
   return w;
 }
 
+// Split of N_k keys into whole 128-key tiles: n_splits requested parts of
+// split_tiles tiles each (the last one ragged); no part is empty.
+struct SplitGeom {
+  int n_kv_tiles, split_tiles, n_splits;
+};
+
+SplitGeom split_geom(int N_k, int n_splits) {
+  SplitGeom g;
+  g.n_kv_tiles = (N_k + 127) / 128;
+  const int req = n_splits < g.n_kv_tiles ? n_splits : g.n_kv_tiles;
+  g.split_tiles = (g.n_kv_tiles + req - 1) / req;
+  g.n_splits = (g.n_kv_tiles + g.split_tiles - 1) / g.split_tiles;
+  return g;
+}
+
+struct SplitWorkspace {
+  size_t lse, total;
+};
+
+SplitWorkspace split_workspace(int BH, int N_q, int d_v, int n_splits) {
+  SplitWorkspace w;
+  const size_t rows = (size_t)n_splits * BH * N_q;
+  w.lse = round_up(rows * d_v * 4, 256);
+  w.total = round_up(w.lse + rows * 4, 256);
+  return w;
+}
+
+int check_split(int B, int H, int N_q, int N_k, int n_splits) {
+  if (B < 1 || H < 1 || N_q < 1 || N_k < 1 || n_splits < 1) return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * H >= (1ll << 31) || N_q >= (1 << 24) || N_k >= (1 << 24)) return ATTN_ERR_INVALID_ARG;
+  const SplitGeom g = split_geom(N_k, n_splits);
+  if ((long long)B * H * ((N_q + 127) / 128) * g.n_splits >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// Query tiles per split-KV CTA: one 128-row tile when the queries fit in one
+// (decode), which lets two CTAs share a multiprocessor; else two tiles share
+// each K/V tile load.  d_qk = 192 has only the two-tile layout.
+int split_nqt(int N_q, int d_qk) { return (N_q <= 128 && d_qk <= 128) ? 1 : 2; }
+int split_ctas_per_sm(int nqt) { return nqt == 1 ? 2 : 1; }
+
 }  // namespace
+
+namespace attn {
+
+cudaError_t prepare_kernel(const void* kernel, int smem_bytes, int launch_regs, int* sms) {
+  struct Prepared {
+    const void* kernel;
+    int dev, sms;
+  };
+  static std::mutex mu;
+  static std::vector<Prepared> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Prepared& d : done)
+      if (d.kernel == kernel && d.dev == dev) {
+        if (sms) *sms = d.sms;
+        return cudaSuccess;
+      }
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != launch_regs) return cudaErrorInvalidConfiguration;
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  done.push_back({kernel, dev, n});
+  if (sms) *sms = n;
+  return cudaSuccess;
+}
+
+}  // namespace attn
 
 extern "C" {
 
@@ -242,6 +323,99 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     add_record(0, ea, eb);
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_splitkv_heuristic(int B, int H, int N_q, int N_k, int d_qk, int n_sms) {
+  if (check_split(B, H, N_q, N_k, 1) != ATTN_OK || n_sms < 1 || !fwd_dims_ok(d_qk, d_qk == 192 ? 128 : d_qk))
+    return 0;
+  // units without a split: (b, h, block of nqt 128-row query tiles), and the
+  // CTAs that run at once
+  const int nqt = split_nqt(N_q, d_qk);
+  const long long units = (long long)B * H * (((N_q + 127) / 128 + nqt - 1) / nqt);
+  const long long slots = (long long)n_sms * split_ctas_per_sm(nqt);
+  if (2 * units > slots) return 1;
+  const int n_kv_tiles = (N_k + 127) / 128;
+  // the largest power of two that keeps every part in one wave (a second,
+  // partial wave costs as much as the first), each part at least two key
+  // tiles long
+  long long n = 1;
+  while (2 * n * units <= slots) n *= 2;
+  const int max_parts = n_kv_tiles / 2 > 1 ? n_kv_tiles / 2 : 1;
+  if (n > max_parts) n = max_parts;
+  return split_geom(N_k, (int)n).n_splits;
+}
+
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N_q, int N_k, int d_v, int n_splits) {
+  if (check_split(B, H, N_q, N_k, n_splits) != ATTN_OK || (d_v != 64 && d_v != 128)) return 0;
+  return split_workspace(B * H, N_q, d_v, split_geom(N_k, n_splits).n_splits).total;
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
+                     int N_k, int d_qk, int d_v, float scale, int n_splits, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (int st = check_split(B, H, N_q, N_k, n_splits)) return st;
+  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!fwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  const int BH = B * H;
+  const SplitGeom g = split_geom(N_k, n_splits);
+  const SplitWorkspace w = split_workspace(BH, N_q, d_v, g.n_splits);
+  if (workspace == nullptr || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  const Settings cfg = settings();
+  attn::FwdParams p;
+  memset(&p, 0, sizeof(p));
+  if (int st = make_map(&p.tm_q, q, BH, N_q, d_qk)) return st;
+  if (int st = make_map(&p.tm_k, k, BH, N_k, d_qk)) return st;
+  if (int st = make_map(&p.tm_v, v, BH, N_k, d_v)) return st;
+  if (int st = status_ptr(&p.status)) return st;
+  char* ws = static_cast<char*>(workspace);
+  p.o_part = reinterpret_cast<float*>(ws);
+  p.lse_part = reinterpret_cast<float*>(ws + w.lse);
+  p.rescale_counter = cfg.rescale_counter;
+  p.timeout_ns = cfg.timeout_ns;
+  p.N = N_q;
+  p.Nk = N_k;
+  p.BH = BH;
+  p.n_qtiles = (N_q + 127) / 128;
+  p.n_kv_tiles = g.n_kv_tiles;
+  p.n_splits = g.n_splits;
+  p.split_tiles = g.split_tiles;
+  const int nqt = split_nqt(N_q, d_qk);
+  p.n_blocks = BH * ((p.n_qtiles + nqt - 1) / nqt) * g.n_splits;
+  p.persist = 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.tau = cfg.tau;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  if (profiling()) {
+    for (auto& x : ev)
+      if (cudaEventCreate(&x) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaEventRecord(ev[0], stream);
+  }
+  cudaError_t e = attn::launch_fwd_split(p, d_qk, nqt, stream);
+  if (ev[0] != nullptr) cudaEventRecord(ev[1], stream);
+  // the merge is a programmatic dependent launch unless events sit between
+  if (e == cudaSuccess)
+    e = attn::launch_merge(p.o_part, p.lse_part, g.n_splits, o, lse, BH, N_q, d_v, stream,
+                          cfg.merge_pdl && ev[0] == nullptr);
+  if (ev[0] != nullptr) {
+    cudaEventRecord(ev[2], stream);
+    add_record(4, ev[0], ev[1]);
+    add_record(5, ev[1], ev[2]);
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int BH, int N,
+               int d_v, cudaStream_t stream) {
+  if (!o_parts || !lse_parts || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (n_parts < 1 || BH < 1 || N < 1 || (long long)BH * N >= (1ll << 33)) return ATTN_ERR_INVALID_ARG;
+  if (d_v != 64 && d_v != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  return attn::launch_merge(o_parts, lse_parts, n_parts, o, lse, BH, N, d_v, stream, false) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
 }
 
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d_qk, int d_v, int deterministic) {
@@ -363,10 +537,12 @@ int attn_profile_stop(attn_kernel_times_t* out) {
       case 0: out->launches_fwd++; out->ms_fwd += ms; break;
       case 1: out->launches_bwd_pre++; out->ms_bwd_pre += ms; break;
       case 2: out->launches_bwd_main++; out->ms_bwd_main += ms; break;
-      default: out->launches_bwd_convert++; out->ms_bwd_convert += ms; break;
+      case 3: out->launches_bwd_convert++; out->ms_bwd_convert += ms; break;
+      case 4: out->launches_fwd_split++; out->ms_fwd_split += ms; break;
+      default: out->launches_merge++; out->ms_merge += ms; break;
     }
     to_free.push_back(r.a);
-    if (r.kind == 0 || r.kind == 3) to_free.push_back(r.b);
+    if (r.kind == 0 || r.kind == 3 || r.kind == 5) to_free.push_back(r.b);
   }
   for (cudaEvent_t e : to_free) cudaEventDestroy(e);
   return st;

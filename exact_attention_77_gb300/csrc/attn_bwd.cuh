@@ -677,14 +677,10 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
   }
   if (!paired) {
     auto kernel = bwd_kernel<D, CAUSAL, DET>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-    if (e != cudaSuccess) return e;
     // setmaxnreg.inc waits for registers the dec released: the split must
     // match what the launch hands out
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kernel);
+    cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, nullptr);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != L::kLaunchRegs) return cudaErrorInvalidConfiguration;
     kernel<<<p.BH * p.n_tiles, L::kThreads, L::kSmemBytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

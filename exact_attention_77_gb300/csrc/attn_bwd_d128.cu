@@ -7,12 +7,8 @@ template <bool CAUSAL, bool DET>
 cudaError_t launch_bwd2_main(const BwdParams& p, cudaStream_t stream) {
   using L = Bwd2Layout;
   auto kernel = bwd2_kernel<CAUSAL, DET>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, nullptr);
   if (e != cudaSuccess) return e;
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kernel);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != L::kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int n_pairs = (p.n_tiles + 1) / 2;
   kernel<<<p.BH * n_pairs * 2, L::kThreads, L::kSmemBytes, stream>>>(p);  // clusters of two (kernel attribute)
   return cudaGetLastError();

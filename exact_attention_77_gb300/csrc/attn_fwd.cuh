@@ -93,7 +93,11 @@ enum : int {
   kWhereSmS = 30, kWhereSmO = 31, kWhereSmFinal = 32, kWhereAlign = 1
 };
 
-template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool PERSIST>
+// SPLIT (non-causal only): each unit also takes one of p.n_splits ranges of
+// p.split_tiles key tiles, keys come from a sequence of p.Nk rows, and the
+// epilogue writes the range's normalised FP32 output and LSE to p.o_part /
+// p.lse_part for the merge kernel (split-KV for decode-shaped problems).
+template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool PERSIST, bool SPLIT = false>
 __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<DQK, DV, NQT>::kMinBlocks)
     fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<DQK, DV, NQT>;
@@ -116,11 +120,23 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
   // the K/V ring position carry over), so the next unit's Q, K and V load
   // and its first products issue while this unit's epilogue runs.
   const int n_qblocks = (p.n_qtiles + NQT - 1) / NQT;
+  static_assert(!(SPLIT && CAUSAL), "split-KV is non-causal");
+  const int n_kv_tiles = SPLIT ? p.n_kv_tiles : p.n_qtiles;
+  const int n_keys = SPLIT ? p.Nk : p.N;
   struct Unit {
-    int bh, qblock, nkv[NQT], nkv_max;
+    int bh, qblock, nkv[NQT], nkv_max, j0, split;
   };
   auto unit_at = [&](int u) {
     Unit w;
+    w.j0 = 0;
+    w.split = 0;
+    int kv_len = n_kv_tiles;
+    if (SPLIT) {  // the splits of one query block are neighbours
+      w.split = u % p.n_splits;
+      u /= p.n_splits;
+      w.j0 = w.split * p.split_tiles;
+      kv_len = min(n_kv_tiles - w.j0, p.split_tiles);
+    }
     if (CAUSAL) {  // longest rows first, spread over heads
       const int rank = u / p.BH;
       w.bh = u - rank * p.BH;
@@ -133,7 +149,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
 #pragma unroll
     for (int t = 0; t < NQT; ++t) {
       const int qt = w.qblock * NQT + t;
-      w.nkv[t] = qt < p.n_qtiles ? (CAUSAL ? qt + 1 : p.n_qtiles) : 0;
+      w.nkv[t] = qt < p.n_qtiles ? (CAUSAL ? qt + 1 : kv_len) : 0;
       w.nkv_max = w.nkv[t] > w.nkv_max ? w.nkv[t] : w.nkv_max;
     }
     return w;
@@ -174,6 +190,9 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the merge kernel (a programmatic dependent launch) may be scheduled now;
+  // it waits for this grid's completion before reading the partials
+  if (SPLIT && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp < 4) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(L::kCtlRegs));
@@ -214,12 +233,12 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
 #pragma unroll
               for (int c = 0; c < DQK / 64; ++c)
-                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * 64, j * kTile, w.bh, bar(L::kBarKVFull + s));
+                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * 64, (w.j0 + j) * kTile, w.bh, bar(L::kBarKVFull + s));
             } else {
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kVBytes);
 #pragma unroll
               for (int c = 0; c < DV / 64; ++c)
-                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * 64, j * kTile, w.bh, bar(L::kBarKVFull + s));
+                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * 64, (w.j0 + j) * kTile, w.bh, bar(L::kBarKVFull + s));
             }
             issued = ld + 1;
           }
@@ -429,9 +448,9 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       } else {
         tmem_ld128(tS, s);
       }
-      const int kbase = j * kTile;
-      if ((CAUSAL && j == qt) || kbase + kTile > p.N) {
-        const int lim = CAUSAL ? min(q_row + 1, p.N) : p.N;  // keys < lim are visible
+      const int kbase = (w.j0 + j) * kTile;
+      if ((CAUSAL && j == qt) || kbase + kTile > n_keys) {
+        const int lim = CAUSAL ? min(q_row + 1, p.N) : n_keys;  // keys < lim are visible
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (kbase + c >= lim) s[c] = -INFINITY;
@@ -498,27 +517,48 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const bool live = q_row < p.N;
-        uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                               ((size_t)bh * p.N + (live ? q_row : 0)) * DV);
+        if constexpr (SPLIT) {  // this key range's normalised output and LSE, FP32
+          const size_t prow = ((size_t)w.split * p.BH + bh) * p.N + (live ? q_row : 0);
+          float4* orow4 = reinterpret_cast<float4*>(p.o_part + prow * DV);
 #pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 32) {
-          float o[32];
-          tmem_ld32(tO + c0, o);
-          uint32_t pk[16];
+          for (int c0 = 0; c0 < DV; c0 += 32) {
+            float o[32];
+            tmem_ld32(tO + c0, o);
+            if (live) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
-          if (live) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              for (int v = 0; v < 8; ++v)
+                orow4[c0 / 4 + v] = make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l, o[4 * v + 2] * inv_l,
+                                                o[4 * v + 3] * inv_l);
+            }
           }
+          if (PERSIST) {
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarOFree + t));
+          }
+          if (live) p.lse_part[prow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        } else {
+          uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                                 ((size_t)bh * p.N + (live ? q_row : 0)) * DV);
+#pragma unroll
+          for (int c0 = 0; c0 < DV; c0 += 32) {
+            float o[32];
+            tmem_ld32(tO + c0, o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+            if (live) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+          }
+          // O_t has been read out: the next unit's products may overwrite it
+          if (PERSIST) {
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarOFree + t));
+          }
+          if (live) p.lse[(size_t)bh * p.N + q_row] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
-        // O_t has been read out: the next unit's products may overwrite it
-        if (PERSIST) {
-          tc_fence_before();
-          mbar_arrive(bar(L::kBarOFree + t));
-        }
-        if (live) p.lse[(size_t)bh * p.N + q_row] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
     cbit ^= (uint32_t)(n & 1);
@@ -538,6 +578,21 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
   }
 }
 
+// Split-KV forward (persistent, non-causal, hardware exponentials) followed
+// by the merge kernel (attn_merge.cuh).
+template <int DQK, int DV, int NQT>
+cudaError_t launch_fwd_split_instance(const FwdParams& p, cudaStream_t stream) {
+  using L = FwdLayout<DQK, DV, NQT>;
+  auto kernel = fwd_kernel<DQK, DV, NQT, false, 0, true, true>;
+  int sms = 0;
+  cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, &sms);
+  if (e != cudaSuccess) return e;
+  int grid = sms * L::kMinBlocks;
+  if (grid > p.n_blocks) grid = p.n_blocks;
+  kernel<<<grid, L::kThreads, L::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int DQK, int DV, int NQT, bool CAUSAL, int POLY>
 cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<DQK, DV, NQT>;
@@ -546,22 +601,14 @@ cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
   // already balances.  p.max_ctas > 0 forces the persistent grid.
   const bool persist = p.max_ctas > 0 || p.persist;
   auto kernel = persist ? fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, true> : fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, false>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-  if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits until the registers it asks for are free, so the
   // split must add up to what the launch actually hands out
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kernel);
+  int sms = 0;
+  cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, &sms);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != L::kLaunchRegs) return cudaErrorInvalidConfiguration;
   // persistent grid: as many CTAs as fit on the device at once, each looping
   // over work units (p.max_ctas > 0 sets the grid instead, e.g. one unit per
   // CTA when it is at least the number of units)
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
   int grid = !persist ? p.n_blocks : p.max_ctas > 0 ? p.max_ctas : sms * L::kMinBlocks;
   if (grid > p.n_blocks) grid = p.n_blocks;
   kernel<<<grid, L::kThreads, L::kSmemBytes, stream>>>(p);

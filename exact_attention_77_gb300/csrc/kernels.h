@@ -25,6 +25,15 @@ struct FwdParams {
   int n_blocks;  // work units: BH * ceil(n_qtiles / tiles per CTA)
   int max_ctas;  // persistent grid size (0: as many CTAs as fit)
   int persist;   // 1: persistent CTAs looping over units; 0: one CTA per unit
+  // split-KV (attn_fwd_splitkv): keys from a sequence of Nk rows in n_splits
+  // ranges of split_tiles 128-key tiles; partial outputs [n_splits, BH, N, d_v]
+  // and LSEs [n_splits, BH, N], FP32
+  int Nk;
+  int n_kv_tiles;
+  int n_splits;
+  int split_tiles;
+  float* o_part;
+  float* lse_part;
   float scale_log2;  // scale * log2(e)
   float tau;         // rescale threshold, log2 units
 };
@@ -68,6 +77,21 @@ struct LaunchEvents {
 cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
 cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
 cudaError_t launch_fwd_d192(const FwdParams& p, bool causal, int nqt, int poly, cudaStream_t s);
+// Once per (kernel, device): raise the kernel's dynamic shared-memory limit
+// to smem_bytes and check that it compiled to launch_regs registers per
+// thread (the setmaxnreg split assumes it; cudaErrorInvalidConfiguration
+// otherwise).  *sms (may be null) receives the device's multiprocessor count.
+cudaError_t prepare_kernel(const void* kernel, int smem_bytes, int launch_regs, int* sms);
+
+// nqt: query tiles per CTA (1 only for d_qk <= 128)
+cudaError_t launch_fwd_split(const FwdParams& p, int d_qk, int nqt, cudaStream_t s);
+
+// Merge of split partials: [n_parts, BH, N, d_v] FP32 outputs and [n_parts,
+// BH, N] LSEs into bf16 O [BH, N, d_v] and FP32 LSE [BH, N].
+// pdl: launch as a programmatic dependent of the previous kernel on s (the
+// merge waits for that kernel's completion inside, griddepcontrol.wait).
+cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int BH,
+                         int N, int d_v, cudaStream_t s, bool pdl);
 
 // Backward: preprocess, main, dQ conversion.
 cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s, const LaunchEvents* ev);

@@ -100,6 +100,70 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Split-KV forward ("Attention at Scale -- From FlashAttention to
+ * FlashAttention-4": the FlashInfer section's associative merge of attention
+ * over disjoint key sets, and the "Sequence-Aware Split Heuristic" section's
+ * split of the key sequence over thread blocks when B * H is too small to
+ * fill the GPU, e.g. in decode).  Non-causal attention of N_q queries over
+ * N_k keys:
+ *   q [B,H,N_q,d_qk], k [B,H,N_k,d_qk], v [B,H,N_k,d_v]   bf16, read only
+ *   o [B,H,N_q,d_v] bf16 and lse [B,H,N_q] fp32, written as by attn_fwd
+ *   n_splits        requested number of key ranges (>= 1).  The keys are cut
+ *                   into ceil(N_k/128) tiles of 128 and the tiles into ranges
+ *                   of ceil(tiles / min(n_splits, tiles)) tiles, the last one
+ *                   ragged, so that no range is empty; the number of ranges
+ *                   used can be below n_splits.
+ *   workspace       device memory of at least attn_fwd_splitkv_workspace_bytes
+ *                   bytes, 16-byte aligned, caller-owned, clobbered: the
+ *                   ranges' FP32 outputs and LSEs.
+ * Two kernels run on ``stream``: the forward kernel computes every (b, h,
+ * query block, key range) part, then the merge (attn_merge) combines the
+ * parts of each row; the merge is launched as a programmatic dependent launch
+ * (it starts while the forward drains and waits for its results inside), or
+ * as an ordinary launch where the stream does not allow that.  The head dims are attn_fwd's.  Returns ATTN_OK or an
+ * argument / launch error.
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
+                     int N_k, int d_qk, int d_v, float scale, int n_splits, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/*
+ * Workspace bytes attn_fwd_splitkv needs for these sizes and this requested
+ * n_splits (0 for arguments it rejects): 4 * R * (d_v + 1) rounded up, with
+ * R = ranges used * B * H * N_q.
+ */
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N_q, int N_k, int d_v, int n_splits);
+
+/*
+ * Number of key ranges for attn_fwd_splitkv on a GPU with n_sms
+ * multiprocessors, following the sequence-aware split heuristic.  The
+ * forward runs (b, h, query block) units: blocks of one 128-row query tile
+ * when N_q <= 128 and d_qk <= 128 (two CTAs per multiprocessor), else of two
+ * tiles (one CTA per multiprocessor); S = n_sms times the CTAs per
+ * multiprocessor.  With U units, the answer is the largest power of two n
+ * with n * U <= S (1 when 2U > S), so that every part runs in one wave,
+ * capped so each range is at least two key tiles long.  Pure host
+ * computation.  Returns 0 for invalid arguments (including a d_qk attn_fwd
+ * does not support).
+ */
+int attn_splitkv_heuristic(int B, int H, int N_q, int N_k, int d_qk, int n_sms);
+
+/*
+ * Merge of attention partials over disjoint key sets (the associative merge
+ * operator of the FlashInfer section cited above): for every row r,
+ *   LSE_r = log sum_s exp(lse_parts[s,r]),
+ *   O_r   = sum_s exp(lse_parts[s,r] - LSE_r) o_parts[s,r,:].
+ *   o_parts [n_parts, BH*N, d_v] fp32 and lse_parts [n_parts, BH*N] fp32
+ *     (natural log; a part with LSE = -inf holds no key and drops out)
+ *   o [BH*N, d_v] bf16 and lse [BH*N] fp32, written (a row whose parts are all
+ *     empty gets O = 0, LSE = -inf)
+ *   n_parts >= 1, BH * N < 2^33, d_v 64 or 128; device pointers 16-byte
+ *   aligned.  Returns ATTN_OK or an argument / launch error.
+ */
+int attn_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int BH, int N,
+               int d_v, cudaStream_t stream);
+
+/*
  * Synchronises ``stream``, then returns and clears the device status word of
  * the current device: ATTN_OK, or the first error a kernel recorded since the
  * last call (ATTN_ERR_TIMEOUT, ATTN_ERR_BOUNDS).  If the stream itself
@@ -168,14 +232,18 @@ int attn_set_bwd_pair(int enable);
  * CUDA events immediately before and after each of its kernel launches, on
  * the launch stream.  attn_profile_stop synchronises those events and fills
  * ``out`` with the launch counts and summed durations (milliseconds) per
- * kernel: the forward kernel, and the backward's preprocess, main and dQ
- * conversion kernels.  Profiling adds host work per call; leave it off
+ * kernel: the forward kernel, the backward's preprocess, main and dQ
+ * conversion kernels, and attn_fwd_splitkv's forward and merge kernels (whose
+ * merge then launches as an ordinary kernel rather than a programmatic
+ * dependent).  Profiling adds host work per call; leave it off
  * otherwise.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG (null out / not started)
  * or ATTN_ERR_CUDA.
  */
 typedef struct {
   int launches_fwd, launches_bwd_pre, launches_bwd_main, launches_bwd_convert;
   float ms_fwd, ms_bwd_pre, ms_bwd_main, ms_bwd_convert;
+  int launches_fwd_split, launches_merge; /* attn_fwd_splitkv's two kernels */
+  float ms_fwd_split, ms_merge;
 } attn_kernel_times_t;
 
 int attn_profile_start(void);

@@ -169,3 +169,44 @@ def attention_inputs_torch(shape: AttentionShape, seed: int = 0, with_do: bool =
         pos += int(np.prod(shp))
         pos += pos % 2
     return out
+
+
+# ----------------------------------------------------------------------------
+# Decode-shaped workloads: N_q queries against N_k keys (split-KV forward).
+@dataclass(frozen=True)
+class DecodeShape:
+    B: int
+    H: int
+    N_q: int
+    N_k: int
+    d_qk: int
+    d_v: int
+
+
+def _decode_sizes(shape: DecodeShape):
+    B, H = shape.B, shape.H
+    return [("q", (B, H, shape.N_q, shape.d_qk)), ("k", (B, H, shape.N_k, shape.d_qk)),
+            ("v", (B, H, shape.N_k, shape.d_v))]
+
+
+def decode_inputs(shape: DecodeShape, seed: int = 0) -> dict:
+    """Q [B,H,N_q,d_qk], K [B,H,N_k,d_qk], V [B,H,N_k,d_v] as bfloat16 bit
+    patterns, drawn in that order from one stream (as ``attention_inputs``)."""
+    out = {}
+    pos = 0
+    for name, shp in _decode_sizes(shape):
+        out[name] = normal_bf16_bits(seed, pos, shp)
+        pos += int(np.prod(shp))
+        pos += pos % 2
+    return out
+
+
+def decode_inputs_torch(shape: DecodeShape, seed: int = 0, device="cuda") -> dict:
+    """``decode_inputs`` as torch.bfloat16 tensors on ``device``."""
+    out = {}
+    pos = 0
+    for name, shp in _decode_sizes(shape):
+        out[name] = normal_bf16_torch(seed, pos, shp, device)
+        pos += int(np.prod(shp))
+        pos += pos % 2
+    return out

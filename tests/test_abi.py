@@ -118,3 +118,69 @@ def test_tuning_setters(lib):
     assert lib.get_lib().attn_selftest_wait_timeout(0, None) == A.ATTN_ERR_INVALID_ARG
     assert lib.get_lib().attn_exp2_probe(None, None, 4, 0, None) == A.ATTN_ERR_INVALID_ARG
     assert lib.get_lib().attn_exp2_probe(0x1000, 0x1000, 4, 7, None) == A.ATTN_ERR_INVALID_ARG
+
+
+def test_splitkv_geometry_and_workspace(lib):
+    A = lib
+    # 1000 keys = 8 tiles; 3 requested ranges -> 3 tiles each -> ranges of 3, 3, 2 tiles
+    rows = 3 * 2 * 5  # ranges * B * H * N_q
+    want = -(-(rows * 128 * 4) // 256) * 256 + rows * 4
+    assert A.attn_fwd_splitkv_workspace_bytes(1, 2, 5, 1000, 128, 3) == -(-want // 256) * 256
+    # more ranges requested than tiles: one range per tile
+    assert A.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 300, 64, 50) == A.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 300, 64, 3)
+    # 8 tiles, 5 requested -> 2 tiles each -> 4 ranges
+    assert A.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 1000, 64, 5) == A.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 1000, 64, 4)
+    assert A.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 1000, 96, 2) == 0
+    assert A.attn_fwd_splitkv_workspace_bytes(1, 1, 0, 1000, 64, 2) == 0
+    assert A.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 1000, 64, 0) == 0
+
+
+def test_splitkv_heuristic(lib):
+    A = lib
+    h = A.attn_splitkv_heuristic
+    # decode (N_q <= 128, d <= 128): one-tile units, two CTAs per SM -> 296
+    # slots on 148 SMs.  8 units -> 32 ranges (256 <= 296 < 512)
+    assert h(1, 8, 1, 16384, 128, 148) == 32
+    assert h(1, 8, 1, 16384, 128, 152) == 32
+    assert h(1, 16, 1, 16384, 64, 152) == 16
+    # 160 units > 304 / 2: no split
+    assert h(1, 160, 1, 16384, 128, 152) == 1
+    # d = 192: two-tile units, one CTA per SM -> 8 units -> 16 ranges
+    assert h(1, 8, 1, 16384, 192, 152) == 16
+    # 200 queries: two-tile units (1 per head), one CTA per SM -> 128 ranges, capped
+    # at two tiles each: 8192 keys = 64 tiles -> 32 ranges
+    assert h(1, 1, 200, 8192, 128, 152) == 32
+    # short key sequences: each range at least two tiles
+    assert h(1, 1, 1, 1024, 128, 148) == 4
+    assert h(1, 1, 1, 128, 128, 148) == 1
+    assert h(1, 1, 1, 0, 128, 148) == 0
+    assert h(1, 1, 1, 100, 128, 0) == 0
+    assert h(1, 1, 1, 100, 96, 148) == 0
+
+
+def test_splitkv_and_merge_argument_errors(lib):
+    A = lib
+    f = lib.get_lib().attn_fwd_splitkv
+    p = 0x1000
+    ws = A.attn_fwd_splitkv_workspace_bytes(1, 2, 1, 1000, 128, 4)
+    args = dict(q=p, k=p, v=p, o=p, lse=p, B=1, H=2, Nq=1, Nk=1000, dqk=128, dv=128, scale=0.1, ns=4, w=p, wb=ws)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"], a["dqk"], a["dv"],
+                 a["scale"], a["ns"], a["w"], a["wb"], None)
+
+    assert call(q=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(Nk=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(ns=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == A.ATTN_ERR_INVALID_ARG
+    assert call(dqk=96, dv=96) == A.ATTN_ERR_UNSUPPORTED
+    assert call(v=0x1008) == A.ATTN_ERR_MISALIGNED
+    assert call(w=None) == A.ATTN_ERR_WORKSPACE
+    assert call(wb=ws - 1) == A.ATTN_ERR_WORKSPACE
+    assert call(w=0x1004) == A.ATTN_ERR_MISALIGNED
+    m = lib.get_lib().attn_merge
+    assert m(p, p, 0, p, p, 1, 1, 128, None) == A.ATTN_ERR_INVALID_ARG
+    assert m(p, None, 2, p, p, 1, 1, 128, None) == A.ATTN_ERR_INVALID_ARG
+    assert m(p, p, 2, p, p, 1, 1, 192, None) == A.ATTN_ERR_UNSUPPORTED
+    assert m(p, 0x1004, 2, p, p, 1, 1, 128, None) == A.ATTN_ERR_MISALIGNED

@@ -49,3 +49,16 @@ def test_torch_generator_matches_numpy_on_cpu():
     for name in a:
         bits = b[name].view(torch.int16).numpy().view(np.uint16)
         np.testing.assert_array_equal(bits, a[name])
+
+
+def test_decode_inputs_order_and_shapes():
+    s = synth.DecodeShape(1, 2, 3, 10, 4, 6)
+    t = synth.decode_inputs(s, seed=0)
+    assert t["q"].shape == (1, 2, 3, 4) and t["k"].shape == (1, 2, 10, 4) and t["v"].shape == (1, 2, 10, 6)
+    np.testing.assert_array_equal(t["k"], synth.normal_bf16_bits(0, 24, (1, 2, 10, 4)))
+    np.testing.assert_array_equal(t["v"], synth.normal_bf16_bits(0, 104, (1, 2, 10, 6)))
+
+    torch = __import__("pytest").importorskip("torch")
+    b = synth.decode_inputs_torch(s, seed=0, device="cpu")
+    for name in t:
+        np.testing.assert_array_equal(b[name].view(torch.int16).numpy().view(np.uint16), t[name])
