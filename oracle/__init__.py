@@ -16,6 +16,9 @@ exp2_poly   the 2^x polynomial emulation: our own minimax fit and its error
 roofline    the cycle model behind the forward and backward roofline tables.
 merge       attention over a key range (split-KV partials) and the associative
             merge of such partials.
+fp8         the e4m3 format, the Hadamard rotation of Q and K, power-of-two
+            block scales, and the FP8 forward (online softmax with P
+            rounded to e4m3) from quantised inputs.
 
 Every function is pinned by a CPU test against something other than itself
 (brute force, finite differences, closed forms, invariants, or the numbers
