@@ -45,6 +45,9 @@ _SIGS = {
     "attn_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "attn_splitkv_heuristic": (_I, [_I, _I, _I, _I, _I, _I]),
     "attn_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _P]),
+    "attn_fp8_quantize_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
+    "attn_fp8_quantize": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
+    "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_profile_start": (_I, []),
     "attn_profile_stop": (_I, [_P]),
 }
@@ -159,6 +162,30 @@ def attn_splitkv_heuristic(B, H, N_q, N_k, d_qk, n_sms) -> int:
 def attn_merge(o_parts, lse_parts, n_parts, o, lse, BH, N, d_v, stream=None, check=True) -> int:
     st = get_lib().attn_merge(_ptr(o_parts), _ptr(lse_parts), int(n_parts), _ptr(o), _ptr(lse), BH, N, d_v,
                               _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_fp8_quantize_workspace_bytes(B, H) -> int:
+    return get_lib().attn_fp8_quantize_workspace_bytes(B, H)
+
+
+def attn_fp8_quantize(q, k, v, signs, q8, k8, v8, sq, sk, sv, B, H, N, d, workspace, workspace_bytes, stream=None,
+                      check=True) -> int:
+    """``signs``: a host sequence of d values, each +1 or -1."""
+    arr = (ctypes.c_byte * len(signs))(*[int(x) for x in signs])
+    st = get_lib().attn_fp8_quantize(_ptr(q), _ptr(k), _ptr(v), ctypes.cast(arr, _P), _ptr(q8), _ptr(k8), _ptr(v8),
+                                     _ptr(sq), _ptr(sk), _ptr(sv), B, H, N, d, _ptr(workspace), int(workspace_bytes),
+                                     _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, B, H, N, d, causal, scale, stream=None, check=True) -> int:
+    st = get_lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o), _ptr(lse), B, H,
+                                N, d, int(causal), float(scale), _stream(stream))
     if check:
         _check(st)
     return st

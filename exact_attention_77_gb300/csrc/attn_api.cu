@@ -29,6 +29,7 @@ struct Settings {
   int fwd_persist = -1;  // -1: by sequence length; 0 / 1 forces
   int bwd_pair = 0;      // 1: d = 128 backward on CTA pairs
   int merge_pdl = 1;     // 1: split-KV merge as a programmatic dependent launch
+  float fp8_tau = 4.f;   // FP8 forward: rescale threshold (P stored as e4m3(2^(8 - tau) P))
   float tau = 8.0f;
   unsigned long long* rescale_counter = nullptr;
 };
@@ -79,6 +80,10 @@ Settings settings() {
     if (const char* e = getenv("ATTN_FWD_PERSIST")) g_settings.fwd_persist = atoi(e);
     if (const char* e = getenv("ATTN_BWD_PAIR")) g_settings.bwd_pair = atoi(e) != 0;
     if (const char* e = getenv("ATTN_MERGE_PDL")) g_settings.merge_pdl = atoi(e) != 0;
+    if (const char* e = getenv("ATTN_FP8_TAU")) {
+      const int v = atoi(e);
+      if (v >= 0 && v <= 8) g_settings.fp8_tau = (float)v;
+    }
   }
   return g_settings;
 }
@@ -112,16 +117,18 @@ int encoder(EncodeTiledFn* out) {
   return ATTN_OK;
 }
 
-// 3-D view [BH, N, d] of a contiguous bf16 tensor; box 64 (d) x 128 (rows) x 1
-// with the 128-byte swizzle; rows past N read as zero.
-int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128) {
+// 3-D view [BH, N, d] of a contiguous tensor of bf16 (elem_bytes 2) or of
+// 8-bit codes (elem_bytes 1); box 128 bytes of d x box_rows rows x 1 with the
+// 128-byte swizzle; rows past N read as zero.
+int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128, int elem_bytes = 2) {
   EncodeTiledFn enc;
   if (int st = encoder(&enc)) return st;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * elem_bytes, (cuuint64_t)N * d * elem_bytes};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = enc(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
@@ -132,7 +139,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_common(int B, int H, int N, float scale, int causal) {
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if ((long long)B * H >= (1ll << 31) || N >= (1 << 24)) return ATTN_ERR_INVALID_ARG;
-  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  // the running max is taken as max(S) * scale: the scale must not be negative
+  if (!isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
@@ -355,7 +363,7 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (int st = check_split(B, H, N_q, N_k, n_splits)) return st;
-  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
   if (!fwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
   const int BH = B * H;
@@ -403,6 +411,93 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
     cudaEventRecord(ev[2], stream);
     add_record(4, ev[0], ev[1]);
     add_record(5, ev[1], ev[2]);
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_fp8_quantize_workspace_bytes(int B, int H) {
+  if (B < 1 || H < 1 || (long long)B * H >= (1ll << 31)) return 0;
+  return round_up((size_t)B * H * 4, 256);
+}
+
+int attn_fp8_quantize(const void* q, const void* k, const void* v, const signed char* signs, void* q8, void* k8,
+                      void* v8, float* sq, float* sk, float* sv, int B, int H, int N, int d, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !signs || !q8 || !k8 || !v8 || !sq || !sk || !sv) return ATTN_ERR_INVALID_ARG;
+  if (int st = check_common(B, H, N, 1.0f, 0)) return st;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  const int n_tiles = (N + 127) / 128;
+  if ((long long)B * H * n_tiles >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  attn::QuantParams p;
+  memset(&p, 0, sizeof(p));
+  for (int i = 0; i < d; ++i) {
+    if (signs[i] != 1 && signs[i] != -1) return ATTN_ERR_INVALID_ARG;
+    if (signs[i] < 0) p.signs[i / 32] |= 1u << (i % 32);
+  }
+  const void* ptrs[] = {q, k, v, q8, k8, v8, sq, sk, sv};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return ATTN_ERR_MISALIGNED;
+  if (workspace == nullptr || workspace_bytes < attn_fp8_quantize_workspace_bytes(B, H)) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.q8 = static_cast<uint8_t*>(q8);
+  p.k8 = static_cast<uint8_t*>(k8);
+  p.v8 = static_cast<uint8_t*>(v8);
+  p.sq = sq;
+  p.sk = sk;
+  p.sv = sv;
+  p.vmax = static_cast<unsigned*>(workspace);
+  p.BH = B * H;
+  p.N = N;
+  p.n_tiles = n_tiles;
+  return attn::launch_fp8_quantize(p, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk, const float* sv,
+                 void* o, float* lse, int B, int H, int N, int d, int causal, float scale, cudaStream_t stream) {
+  if (!q8 || !k8 || !v8 || !sq || !sk || !sv || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (int st = check_common(B, H, N, scale, causal)) return st;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q8, k8, v8, sq, sk, sv, o, lse};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return ATTN_ERR_MISALIGNED;
+  const Settings cfg = settings();
+  attn::FwdParams p;
+  memset(&p, 0, sizeof(p));
+  const int BH = B * H;
+  if (int st = make_map(&p.tm_q, q8, BH, N, d, 128, 1)) return st;
+  if (int st = make_map(&p.tm_k, k8, BH, N, d, 128, 1)) return st;
+  if (int st = make_map(&p.tm_v, v8, BH, N, d, 128, 1)) return st;
+  if (int st = status_ptr(&p.status)) return st;
+  p.o = o;
+  p.lse = lse;
+  p.sq = sq;
+  p.sk = sk;
+  p.sv = sv;
+  p.rescale_counter = cfg.rescale_counter;
+  p.timeout_ns = cfg.timeout_ns;
+  p.N = N;
+  p.BH = BH;
+  p.n_qtiles = (N + 127) / 128;
+  p.n_blocks = BH * ((p.n_qtiles + 1) / 2);
+  p.max_ctas = cfg.fwd_max_ctas;
+  p.persist = cfg.fwd_persist >= 0 ? cfg.fwd_persist : (N <= 4096 ? 1 : 0);
+  // the codes hold (x sqrt(d) R) / s: the scores carry a factor d
+  p.scale_log2 = scale * 1.4426950408889634f / (float)d;
+  // P (<= 2^tau against the stale max) is stored as e4m3(2^(8 - tau) P)
+  p.tau = cfg.fp8_tau;
+  p.p_off = 8.f - cfg.fp8_tau;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  if (profiling()) {
+    if (cudaEventCreate(&ea) != cudaSuccess || cudaEventCreate(&eb) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaEventRecord(ea, stream);
+  }
+  const cudaError_t e = attn::launch_fwd_fp8(p, causal != 0, stream);
+  if (ea != nullptr) {
+    cudaEventRecord(eb, stream);
+    add_record(0, ea, eb);
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

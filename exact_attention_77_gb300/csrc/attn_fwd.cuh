@@ -38,16 +38,23 @@
 namespace attn {
 
 constexpr int kTile = 128;
-constexpr int kSubTile = 128 * 128;  // bytes: 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr int kSubTile = 128 * 128;  // bytes: 128 rows x 128 B (one 128-byte swizzle span: 64 bf16 or 128 e4m3)
 // Of every 32 score columns, this many take the polynomial exponential and the
 // rest the hardware unit (the "poly" kernel variants; 0 = hardware only).
 constexpr int kPolyCols = 10;
 
-template <int DQK, int DV, int NQT>
+// ES: bytes per operand element (2: bf16; 1: e4m3).
+template <int DQK, int DV, int NQT, int ES = 2>
 struct FwdLayout {
-  static constexpr int kQBytes = kTile * DQK * 2;
-  static constexpr int kKBytes = kTile * DQK * 2;
-  static constexpr int kVBytes = kTile * DV * 2;
+  static constexpr int kQBytes = kTile * DQK * ES;
+  static constexpr int kKBytes = kTile * DQK * ES;
+  static constexpr int kVBytes = kTile * DV * ES;
+  static constexpr int kChunkElems = 128 / ES;        // elements per 128-byte swizzle span
+  static constexpr int kChunksQK = DQK * ES / 128;
+  static constexpr int kChunksV = DV * ES / 128;
+  static constexpr int kQKSteps = DQK * ES / 32;      // products of K = 32 bytes per S tile
+  static constexpr int kPVSteps = kTile * ES / 32;    // products per P V (32-byte K steps)
+  static constexpr int kPVKeys = 32 / ES;             // keys per P V product
   static constexpr int kStageBytes = kKBytes > kVBytes ? kKBytes : kVBytes;
   static constexpr int kQRegion = NQT * kQBytes;
   // One query tile per CTA is sized so two CTAs share an SM (two softmax
@@ -97,10 +104,15 @@ enum : int {
 // p.split_tiles key tiles, keys come from a sequence of p.Nk rows, and the
 // epilogue writes the range's normalised FP32 output and LSE to p.o_part /
 // p.lse_part for the merge kernel (split-KV for decode-shaped problems).
-template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool PERSIST, bool SPLIT = false>
+// FP8 (d = 128, POLY = 0): Q, K, V are e4m3 codes with per-tile scales p.sq,
+// p.sk and a per-head scale p.sv; the products run as kind::f8f6f4; the
+// softmax forms 2^8 P against a running max updated on every rise (the host
+// passes tau = 0) and stores it as e4m3 over the first 32 columns of S_t.
+template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool PERSIST, bool SPLIT = false, bool FP8 = false>
 __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<DQK, DV, NQT>::kMinBlocks)
     fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = FwdLayout<DQK, DV, NQT>;
+  using L = FwdLayout<DQK, DV, NQT, FP8 ? 1 : 2>;
+  static_assert(!FP8 || (DQK == 128 && DV == 128 && POLY == 0 && !SPLIT), "FP8 instance: d = 128, MUFU only");
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -214,9 +226,9 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
 #pragma unroll
         for (int t = 0; t < NQT; ++t)
 #pragma unroll
-          for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(sbase + t * L::kQBytes + c * kSubTile, &p.tm_q, c * 64, (w.qblock * NQT + t) * kTile, w.bh,
-                        bar(L::kBarQFull));
+          for (int c = 0; c < L::kChunksQK; ++c)
+            tma_load_3d(sbase + t * L::kQBytes + c * kSubTile, &p.tm_q, c * L::kChunkElems,
+                        (w.qblock * NQT + t) * kTile, w.bh, bar(L::kBarQFull));
         ++qn;
         for (int j = 0; ok && j < w.nkv_max; ++j) {
 #pragma unroll
@@ -232,13 +244,15 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
             if (h == 0) {
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
 #pragma unroll
-              for (int c = 0; c < DQK / 64; ++c)
-                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * 64, (w.j0 + j) * kTile, w.bh, bar(L::kBarKVFull + s));
+              for (int c = 0; c < L::kChunksQK; ++c)
+                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * L::kChunkElems, (w.j0 + j) * kTile, w.bh,
+                            bar(L::kBarKVFull + s));
             } else {
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kVBytes);
 #pragma unroll
-              for (int c = 0; c < DV / 64; ++c)
-                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * 64, (w.j0 + j) * kTile, w.bh, bar(L::kBarKVFull + s));
+              for (int c = 0; c < L::kChunksV; ++c)
+                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * L::kChunkElems, (w.j0 + j) * kTile, w.bh,
+                            bar(L::kBarKVFull + s));
             }
             issued = ld + 1;
           }
@@ -254,8 +268,8 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     // =========================== MMA issuer =========================
     // The whole warp runs this loop in step (waits included); one elected
     // lane issues every product and commit.
-    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, false, true);
+    constexpr uint32_t kIdescQK = FP8 ? idesc_e4m3_f32(128, 128, false, false) : idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3_f32(128, DV, false, true) : idesc_bf16_f32(128, DV, false, true);
     auto wait_all = [&](uint32_t b, uint32_t parity, int where) -> bool {
       const bool r = __all_sync(0xffffffffu, mbar_wait(b, parity, ctl, where));
       tc_fence_after();
@@ -268,17 +282,26 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       const uint64_t da = sdesc_sw128(sbase + t * L::kQBytes, 16, 1024);
       const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < DQK / 16; ++kk) {
+      for (int kk = 0; kk < L::kQKSteps; ++kk) {
         const uint32_t off = (kk / 4) * kSubTile + (kk % 4) * 32;
-        mma_ss_elect(tmem + t * 256, sdesc_advance(da, off), sdesc_advance(db, off), kIdescQK, kk > 0);
+        if constexpr (FP8)
+          mma_ss_elect_f8(tmem + t * 256, sdesc_advance(da, off), sdesc_advance(db, off), kIdescQK, kk > 0);
+        else
+          mma_ss_elect(tmem + t * 256, sdesc_advance(da, off), sdesc_advance(db, off), kIdescQK, kk > 0);
       }
     };
     auto issue_pv = [&](int t, int stage, bool acc) {
       const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, kSubTile, 1024);
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        mma_ts_elect(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * 2048), kIdescPV,
-                     (acc || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < L::kPVSteps; ++kk) {
+        // A: P over 8 tensor-memory columns per step; B: the step's kPVKeys V rows
+        if constexpr (FP8)
+          mma_ts_elect_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * L::kPVKeys * 128),
+                          kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        else
+          mma_ts_elect(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * L::kPVKeys * 128),
+                       kIdescPV, (acc || kk > 0) ? 1u : 0u);
+      }
     };
     bool ok = true;
     int ld0 = 0;  // ring position of this unit's K_0
@@ -419,7 +442,9 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     const int quad = warp & 3;  // this warp may touch tensor-memory lanes 32*quad .. 32*quad+31
     const uint32_t tS = tmem + ((uint32_t)(quad * 32) << 16) + t * 256;
     const uint32_t tO = tS + 128;
-    const float c_log2 = p.scale_log2;
+    // FP8: 2^(8 - tau) P is stored (P <= 2^tau against the stale max), so
+    // the exponent is taken against m - (8 - tau)
+    const float kPOff = FP8 ? p.p_off : 0.f;
     unsigned rescales = 0;
     bool ok = true;
     uint32_t cbit = 0;  // parity of the S / P / O-done phases of this tile in earlier units
@@ -433,8 +458,11 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     const int qt = w.qblock * NQT + t;
     const int q_row = qt * kTile + quad * 32 + lane;
     float m = -INFINITY;  // running (possibly stale) max, log2 units
-    float l = 0.f;        // running sum of 2^(s*c - m)
+    float l = 0.f;        // running sum of 2^(s*c - m + kPOff)
+    // FP8: the scores carry the query tile's and the key tile's scales
+    const float c_q = FP8 ? p.scale_log2 * p.sq[(size_t)bh * p.n_qtiles + qt] : p.scale_log2;
     for (int j = 0; j < n; ++j) {
+      const float c_log2 = FP8 ? c_q * p.sk[(size_t)bh * n_kv_tiles + w.j0 + j] : c_q;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), cbit ^ (j & 1), ctl, kWhereSmS));
       if (!ok) break;
       if (quad == 0 && lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 9 + 2 * t);
@@ -489,8 +517,24 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       const float m_use = (m == -INFINITY) ? 0.f : m;
       // x = s * scale * log2(e) - m on pairs (packed FP32 FMA), then 2^x
       const float2 c2 = make_float2(c_log2, c_log2);
-      const float2 nm2 = make_float2(-m_use, -m_use);
+      const float2 nm2 = make_float2(kPOff - m_use, kPOff - m_use);
       float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      if constexpr (FP8) {
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float2 x0 = __ffma2_rn(make_float2(s[c0 + i], s[c0 + i + 1]), c2, nm2);
+            const float2 x1 = __ffma2_rn(make_float2(s[c0 + i + 2], s[c0 + i + 3]), c2, nm2);
+            const float2 e0 = make_float2(ex2_mufu(x0.x), ex2_mufu(x0.y));
+            const float2 e1 = make_float2(ex2_mufu(x1.x), ex2_mufu(x1.y));
+            ls[(i >> 2) & 3] = __fadd2_rn(ls[(i >> 2) & 3], __fadd2_rn(e0, e1));
+            pk[i >> 2] = pack_e4m3x4(e0.x, e0.y, e1.x, e1.y);
+          }
+          tmem_st8(tS + c0 / 4, pk);  // P (e4m3, four per column) over the first 32 columns of S
+        }
+      } else {
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t pk[16];
@@ -504,6 +548,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
         }
         tmem_st16(tS + c0 / 2, pk);  // P (bf16 pairs) over the first 64 columns of S
       }
+      }
       const float2 lsum = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
       l += lsum.x + lsum.y;
       tmem_wait_st();
@@ -515,7 +560,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), cbit ^ ((n - 1) & 1), ctl, kWhereSmFinal));
       if (ok) {
         tc_fence_after();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float inv_l = l > 0.f ? (FP8 ? p.sv[bh] : 1.f) / l : 0.f;
         const bool live = q_row < p.N;
         if constexpr (SPLIT) {  // this key range's normalised output and LSE, FP32
           const size_t prow = ((size_t)w.split * p.BH + bh) * p.N + (live ? q_row : 0);
@@ -557,7 +602,8 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
             tc_fence_before();
             mbar_arrive(bar(L::kBarOFree + t));
           }
-          if (live) p.lse[(size_t)bh * p.N + q_row] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          if (live)
+            p.lse[(size_t)bh * p.N + q_row] = l > 0.f ? (m - kPOff + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
       }
     }
@@ -593,14 +639,15 @@ cudaError_t launch_fwd_split_instance(const FwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int DQK, int DV, int NQT, bool CAUSAL, int POLY>
+template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool FP8 = false>
 cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
-  using L = FwdLayout<DQK, DV, NQT>;
+  using L = FwdLayout<DQK, DV, NQT, FP8 ? 1 : 2>;
   // Persistent CTAs pay off when units are short (few K/V tiles each); with
   // long units the one-unit-per-CTA kernel is leaner and the launch order
   // already balances.  p.max_ctas > 0 forces the persistent grid.
   const bool persist = p.max_ctas > 0 || p.persist;
-  auto kernel = persist ? fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, true> : fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, false>;
+  auto kernel = persist ? fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, true, false, FP8>
+                        : fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, false, false, FP8>;
   // setmaxnreg.inc waits until the registers it asks for are free, so the
   // split must add up to what the launch actually hands out
   int sms = 0;

@@ -34,6 +34,12 @@ struct FwdParams {
   int split_tiles;
   float* o_part;
   float* lse_part;
+  // FP8 forward (attn_fwd_fp8): e4m3 scales per (b, h, 128-row tile) of Q
+  // and K, and per (b, h) of V
+  const float* sq;
+  const float* sk;
+  const float* sv;
+  float p_off;  // FP8: P is stored as e4m3(2^p_off P), p_off = 8 - tau
   float scale_log2;  // scale * log2(e)
   float tau;         // rescale threshold, log2 units
 };
@@ -85,6 +91,25 @@ cudaError_t prepare_kernel(const void* kernel, int smem_bytes, int launch_regs, 
 
 // nqt: query tiles per CTA (1 only for d_qk <= 128)
 cudaError_t launch_fwd_split(const FwdParams& p, int d_qk, int nqt, cudaStream_t s);
+
+// FP8 forward (d = 128, two query tiles per CTA) and the quantiser that
+// prepares its inputs (attn_fp8.cu).
+cudaError_t launch_fwd_fp8(const FwdParams& p, bool causal, cudaStream_t s);
+struct QuantParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  uint8_t* q8;
+  uint8_t* k8;
+  uint8_t* v8;
+  float* sq;
+  float* sk;
+  float* sv;
+  unsigned* vmax;     // [BH] scratch: bit patterns of max |V| per head
+  uint32_t signs[4];  // bit i set: coordinate i of Q and K is negated before the Hadamard transform
+  int BH, N, n_tiles;
+};
+cudaError_t launch_fp8_quantize(const QuantParams& p, cudaStream_t s);
 
 // Merge of split partials: [n_parts, BH, N, d_v] FP32 outputs and [n_parts,
 // BH, N] LSEs into bf16 O [BH, N, d_v] and FP32 LSE [BH, N].

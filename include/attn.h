@@ -66,7 +66,7 @@ typedef enum {
  *   lse [B,H,N]    fp32, written: natural-log log-sum-exp of the scaled,
  *                  unmasked scores of each query row (what the backward needs)
  *   causal         0 or 1 (top-left aligned: query i sees keys 0..i)
- *   scale          finite; usually 1/sqrt(d_qk)
+ *   scale          finite and >= 0; usually 1/sqrt(d_qk)
  * Returns ATTN_OK or an argument / launch error (see the enum).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d_qk,
@@ -162,6 +162,59 @@ int attn_splitkv_heuristic(int B, int H, int N_q, int N_k, int d_qk, int n_sms);
  */
 int attn_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int BH, int N,
                int d_v, cudaStream_t stream);
+
+/*
+ * FP8 (e4m3) forward ("FlashAttention 3 and 4: When the Bottleneck Moves",
+ * section 2.2: per-block scales, and a fixed random rotation R of Q and K
+ * before quantising, which leaves every score unchanged since
+ * (QR)(KR)^T = Q K^T).  Two calls: attn_fp8_quantize turns bf16 Q, K, V
+ * into e4m3 codes with scales, attn_fwd_fp8 runs the forward on them.
+ * d_qk = d_v = 128 only.
+ *
+ * Bytes of device workspace attn_fp8_quantize needs (0 for invalid sizes).
+ */
+size_t attn_fp8_quantize_workspace_bytes(int B, int H);
+
+/*
+ * Quantiser.  R = D H / sqrt(d): H the d x d Sylvester-Hadamard matrix
+ * (H_ij = (-1)^popcount(i & j)), D = diag(signs).
+ *   q, k, v        bf16 [B,H,N,d] device, read only
+ *   signs          HOST array of d entries, each +1 or -1 (read during the
+ *                  call); the same signs must be used for every call whose
+ *                  codes meet in one forward
+ *   q8, k8         uint8 [B,H,N,d] device, written: e4m3 codes of
+ *                  (x sqrt(d) R) / s for the rows of Q and K (sqrt(d) R = D H
+ *                  is exact in binary arithmetic)
+ *   v8             uint8 [B,H,N,d] device, written: e4m3 codes of v / s
+ *   sq, sk         fp32 [B,H,ceil(N/128)] device, written: one scale s per
+ *                  128-row tile of Q and of K
+ *   sv             fp32 [B,H] device, written: one scale per (b, h) of V
+ *   workspace      device, >= attn_fp8_quantize_workspace_bytes, clobbered
+ * Scales are powers of two, the smallest with max|x| <= 448 s over the block
+ * (1 for an all-zero block); codes round to nearest even and saturate at
+ * +-448.  Three kernels (a memset of the workspace, the per-head max of |V|,
+ * the quantiser) run on ``stream``.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG
+ * (null pointer, bad sign, sizes), ATTN_ERR_UNSUPPORTED (d != 128),
+ * ATTN_ERR_MISALIGNED, ATTN_ERR_WORKSPACE or ATTN_ERR_CUDA.
+ */
+int attn_fp8_quantize(const void* q, const void* k, const void* v, const signed char* signs, void* q8, void* k8,
+                      void* v8, float* sq, float* sk, float* sv, int B, int H, int N, int d, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * FP8 forward from attn_fp8_quantize's outputs: O = softmax(scale Q K^T
+ * (+ causal mask)) V and LSE as attn_fwd, with the products on e4m3 operands
+ * (FP32 accumulation) and P rounded to e4m3.  The running row max m moves
+ * only when it rises by more than tau = 4 (log2 units; the decision is taken
+ * per group of 32 query rows), so P <= 2^4 against the stale max and
+ * P' = 2^(x - m + 4) <= 2^8 is stored as e4m3(P'); the row sum takes P'
+ * before rounding, and O = s_v (sum P'_e4m3 v8) / sum P'.  (The environment
+ * variable ATTN_FP8_TAU = 0..8, read at first use, changes tau.)
+ *   o bf16 [B,H,N,d], lse fp32 [B,H,N] written; other arguments as attn_fwd.
+ * Returns ATTN_OK or an argument / launch error.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk, const float* sv,
+                 void* o, float* lse, int B, int H, int N, int d, int causal, float scale, cudaStream_t stream);
 
 /*
  * Synchronises ``stream``, then returns and clears the device status word of

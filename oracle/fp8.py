@@ -26,10 +26,13 @@ Readings taken where the pages are silent (each is one line of DESIGN):
   key tile into one accumulator.  A block's scale is the power of two
   s = 2^k with the smallest k such that amax(block) <= 448 s (s = 1 for an
   all-zero block); a value x is stored as e4m3(x / s).
-* P is quantised as well: P' = 2^(x - m + 8), i.e. 256 P with P <= 1 taken
-  against the running max m, then e4m3(P'); the row sum uses P' before
-  rounding.  The running max is updated whenever it rises (no conditional
-  rescale: with a stale max P could reach 2^8 and 256 P would not fit e4m3).
+* P is quantised as well.  With the conditional rescale of section 3.2
+  (threshold tau, log2 units) P taken against the stale max m is at most
+  2^tau, so P' = 2^(x - m + 8 - tau) <= 2^8 is stored as e4m3(P'); the row sum
+  uses P' before rounding.  The library uses tau = 4 (tau = 0: the max moves
+  on every rise).  As in the kernels, the rescale decision is taken per group
+  of 32 consecutive query rows: when any row of the group rose by more than
+  tau, every row of the group moves to its current max.
 """
 from __future__ import annotations
 
@@ -39,7 +42,9 @@ import numpy as np
 
 LOG2E = 1.0 / math.log(2.0)
 E4M3_MAX = 448.0
-P_EXP_OFFSET = 8.0  # P is stored as e4m3(2^8 P)
+P_MAX_LOG2 = 8.0  # P' = 2^(8 - tau) P <= 2^8
+TAU = 4.0  # the library's rescale threshold for the FP8 forward
+ROW_GROUP = 32  # rows that take one rescale decision together
 
 
 def e4m3_decode(code: int) -> float:
@@ -134,20 +139,27 @@ def quantize_qkv(q, k, v, signs, tile: int = 128):
 
 
 def forward_head(q8, k8, v8, sq, sk, sv: float, scale: float, causal: bool, d: int, tile: int = 128,
-                 quantize_p: bool = True):
+                 quantize_p: bool = True, rows=None, tau: float = TAU):
     """FP8 forward of one head from quantised inputs, in FP64.
 
     q8 [Nq, d], k8 [Nk, d], v8 [Nk, d_v] on the e4m3 grid; sq [ceil(Nq/tile)],
     sk [ceil(Nk/tile)] the per-tile scales, sv the head's V scale; ``scale``
     the caller's softmax scale; d the rotated dimension (the 1/d of the
     rotation goes into the scores).  Online softmax over key tiles: scores
-    x = scale/d * sq_i sk_j (q8 k8^T) in log2 units, running max m updated on
-    every rise (acc and l rescaled by 2^(m_old - m)), P' = 2^(x - m + 8)
-    stored as e4m3(P') (or kept exact when quantize_p is False), l += sum P',
-    acc += P' v8.  O = sv acc / l, LSE = (m - 8 + log2 l) ln 2.
+    x = scale/d * sq_i sk_j (q8 k8^T) in log2 units; candidate max
+    m_new = max(m, rowmax x); where any row of a 32-row group has
+    m_new > m + tau (or m is still -inf) the whole group moves to m_new, acc
+    and l scaled by 2^(m - m_new); P' = 2^(x - m + 8 - tau) stored as
+    e4m3(P') (or kept exact when quantize_p is False), l += sum P',
+    acc += P' v8.  O = sv acc / l, LSE = (m - (8 - tau) + log2 l) ln 2.
+    ``rows`` (optional): the query indices of q8's rows within the head, when
+    q8 holds a sample of them (they select the tile scale, the causal mask
+    and the rescale group; a sample must hold whole 32-row groups).
     Returns (O, LSE)."""
     nq, nk = q8.shape[0], k8.shape[0]
-    rows = np.arange(nq)
+    rows = np.arange(nq) if rows is None else np.asarray(rows)
+    _, group = np.unique(rows // ROW_GROUP, return_inverse=True)
+    p_off = P_MAX_LOG2 - tau
     c_row = (scale / d) * LOG2E * np.asarray(sq, dtype=np.float64)[rows // tile]
     m = np.full(nq, -np.inf)
     l = np.zeros(nq)
@@ -158,22 +170,24 @@ def forward_head(q8, k8, v8, sq, sk, sv: float, scale: float, causal: bool, d: i
         if causal:
             x = np.where(np.arange(j0, j1)[None, :] > rows[:, None], -np.inf, x)
         m_new = np.maximum(m, x.max(axis=1))
-        live = np.isfinite(m_new)
-        alpha = np.where(np.isfinite(m), np.exp2(m - np.where(live, m_new, 0.0)), 0.0)
+        rose = np.isfinite(m_new) & (~np.isfinite(m) | (m_new > m + tau))
+        need = np.bincount(group, weights=rose)[group] > 0  # any row of the group
+        alpha = np.where(need & np.isfinite(m), np.exp2(m - np.where(np.isfinite(m_new), m_new, 0.0)), 1.0)
+        alpha = np.where(need & ~np.isfinite(m), 0.0, alpha)
         acc *= alpha[:, None]
         l *= alpha
-        m = m_new
-        m_use = np.where(live, m, 0.0)
-        p = np.exp2(x - m_use[:, None] + P_EXP_OFFSET)
+        m = np.where(need, m_new, m)
+        m_use = np.where(np.isfinite(m), m, 0.0)
+        p = np.exp2(x - m_use[:, None] + p_off)
         l += p.sum(axis=1)
         acc += (e4m3_round(p) if quantize_p else p) @ v8[j0:j1]
     with np.errstate(invalid="ignore", divide="ignore"):
         o = np.where(l[:, None] > 0, sv * acc / np.where(l > 0, l, 1.0)[:, None], 0.0)
-        lse = np.where(l > 0, (m - P_EXP_OFFSET + np.log2(np.where(l > 0, l, 1.0))) / LOG2E, -np.inf)
+        lse = np.where(l > 0, (m - p_off + np.log2(np.where(l > 0, l, 1.0))) / LOG2E, -np.inf)
     return o, lse
 
 
-def forward(qz: dict, scale: float, causal: bool, quantize_p: bool = True):
+def forward(qz: dict, scale: float, causal: bool, quantize_p: bool = True, tau: float = TAU):
     """forward_head over every (b, h) of quantize_qkv's output."""
     q8 = qz["q8"]
     B, H, N, d = q8.shape
@@ -183,7 +197,7 @@ def forward(qz: dict, scale: float, causal: bool, quantize_p: bool = True):
         for h in range(H):
             o[b, h], lse[b, h] = forward_head(q8[b, h], qz["k8"][b, h], qz["v8"][b, h], qz["sq"][b, h],
                                               qz["sk"][b, h], float(qz["sv"][b, h]), scale, causal, d,
-                                              quantize_p=quantize_p)
+                                              quantize_p=quantize_p, tau=tau)
     return o, lse
 
 

@@ -84,6 +84,8 @@ def test_forward_argument_errors(lib):
     assert _fwd(lib, causal=2) == A.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, scale=float("nan")) == A.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, scale=float("inf")) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=-0.125) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0, q=0) == A.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, dqk=96, dv=96) == A.ATTN_ERR_UNSUPPORTED
     assert _fwd(lib, dqk=128, dv=64) == A.ATTN_ERR_UNSUPPORTED
     assert _fwd(lib, k=0x1008) == A.ATTN_ERR_MISALIGNED
@@ -184,3 +186,31 @@ def test_splitkv_and_merge_argument_errors(lib):
     assert m(p, None, 2, p, p, 1, 1, 128, None) == A.ATTN_ERR_INVALID_ARG
     assert m(p, p, 2, p, p, 1, 1, 192, None) == A.ATTN_ERR_UNSUPPORTED
     assert m(p, 0x1004, 2, p, p, 1, 1, 128, None) == A.ATTN_ERR_MISALIGNED
+
+
+def test_fp8_argument_errors(lib):
+    A = lib
+    L = lib.get_lib()
+    p = 0x1000
+    ws = A.attn_fp8_quantize_workspace_bytes(1, 2)
+    assert ws == 256 and A.attn_fp8_quantize_workspace_bytes(0, 2) == 0
+    signs = [1, -1] * 64
+
+    def quant(**kw):
+        a = dict(q=p, k=p, v=p, signs=signs, q8=p, k8=p, v8=p, sq=p, sk=p, sv=p, B=1, H=2, N=300, d=128, w=p, wb=ws)
+        a.update(kw)
+        return A.attn_fp8_quantize(a["q"], a["k"], a["v"], a["signs"], a["q8"], a["k8"], a["v8"], a["sq"], a["sk"],
+                                   a["sv"], a["B"], a["H"], a["N"], a["d"], a["w"], a["wb"], stream=0, check=False)
+
+    assert quant(q=0) == A.ATTN_ERR_INVALID_ARG
+    assert quant(signs=[1] * 127 + [0]) == A.ATTN_ERR_INVALID_ARG
+    assert quant(d=64, signs=[1] * 64) == A.ATTN_ERR_UNSUPPORTED
+    assert quant(sk=0x1004) == A.ATTN_ERR_MISALIGNED
+    assert quant(w=None) == A.ATTN_ERR_WORKSPACE
+    assert quant(wb=ws - 4) == A.ATTN_ERR_WORKSPACE
+    f = L.attn_fwd_fp8
+    assert f(p, p, p, p, p, p, p, p, 1, 2, 300, 128, 0, -1.0, None) == A.ATTN_ERR_INVALID_ARG
+    assert f(p, p, p, p, p, 0, p, p, 1, 2, 300, 128, 0, 0.1, None) == A.ATTN_ERR_INVALID_ARG
+    assert f(p, p, p, p, p, p, p, p, 1, 2, 300, 64, 0, 0.1, None) == A.ATTN_ERR_UNSUPPORTED
+    assert f(p, 0x1001, p, p, p, p, p, p, 1, 2, 300, 128, 0, 0.1, None) == A.ATTN_ERR_MISALIGNED
+    assert f(p, p, p, p, p, p, p, p, 1, 2, 300, 128, 2, 0.1, None) == A.ATTN_ERR_INVALID_ARG

@@ -112,7 +112,8 @@ def _inputs(B, H, N, d, seed, frac=0.0, mag=1.0):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_forward_without_p_rounding_is_exact_attention_of_the_quantised_inputs(causal):
+@pytest.mark.parametrize("tau", [0.0, 4.0, 8.0])
+def test_forward_without_p_rounding_is_exact_attention_of_the_quantised_inputs(causal, tau):
     (q, k, v), signs = _inputs(1, 2, 300, 128, 3)
     # tiles of different magnitudes, so every tile gets its own scale
     q[..., 128:256, :] *= 8.0
@@ -120,7 +121,7 @@ def test_forward_without_p_rounding_is_exact_attention_of_the_quantised_inputs(c
     k[..., 256:, :] *= 4.0
     qz = fp8.quantize_qkv(q, k, v, signs)
     assert len(set(qz["sq"][0, 0].tolist())) == 2 and len(set(qz["sk"][0, 0].tolist())) == 3
-    o, lse = fp8.forward(qz, 0.09, causal, quantize_p=False)
+    o, lse = fp8.forward(qz, 0.09, causal, quantize_p=False, tau=tau)
     # dequantised, un-rotated: Q8 sq (sqrt(d) R)^T etc.; the scores equal those
     # of the dequantised rotated tensors divided by d
     tile_q = np.repeat(qz["sq"], 128, axis=-1)[..., :300, None]
@@ -175,3 +176,26 @@ def test_rotation_reduces_the_error_on_outlier_inputs():
     assert 0.9 < rmse(0.0, 1.0, 6) < 1.1
     assert rmse(0.001, 10.0, 7) > 1.3
     assert rmse(0.01, 10.0, 8) > 1.8
+
+
+def test_stale_max_keeps_p_within_the_format():
+    """With threshold tau = 4 the stored P' = 2^(8 - tau) P never exceeds 2^8
+    (no saturation), and on a rising-max input it does exceed 2^4, i.e. P is
+    taken against a stale max."""
+    (q, k, v), signs = _inputs(1, 1, 512, 128, 9)
+    # a rising max: later keys score higher
+    k *= np.linspace(0.2, 3.0, 512)[None, None, :, None]
+    qz = fp8.quantize_qkv(q, k, v, signs)
+    seen = []
+    saved = fp8.e4m3_round
+
+    def spy(x):
+        seen.append(float(np.max(x)))
+        return saved(x)
+
+    try:
+        fp8.e4m3_round = spy
+        fp8.forward(qz, 1 / math.sqrt(128), False, tau=4.0)
+    finally:
+        fp8.e4m3_round = saved
+    assert max(seen) <= 256.0 and max(seen) > 16.0
