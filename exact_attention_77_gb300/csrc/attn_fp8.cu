@@ -23,7 +23,8 @@ namespace attn {
 
 namespace {
 
-constexpr int kQuantRowsPerWarp = 16;  // 8 warps x 16 rows = one 128-row tile
+constexpr int kQuantWarps = 16;
+constexpr int kQuantRowsPerWarp = kTile / kQuantWarps;  // 16 warps x 8 rows = one 128-row tile
 
 // Smallest power-of-two exponent k with amax <= 448 * 2^k (0 for amax = 0):
 // with amax = f 2^e, f in [0.5, 1), and 448 = 0.875 2^9.
@@ -35,16 +36,23 @@ __device__ __forceinline__ int pow2_scale_exp(float amax) {
 }
 
 // max |V| over one 128-row tile, folded into vmax[bh] (non-negative floats
-// order like their bit patterns).
+// order like their bit patterns).  Each thread takes 8 of the tile's 2048
+// 16-byte chunks, all loads in flight together.
 __global__ void __launch_bounds__(256) v_amax_kernel(const QuantParams p) {
   const int tile = blockIdx.x % p.n_tiles, bh = blockIdx.x / p.n_tiles;
   const int rows = min(kTile, p.N - tile * kTile);
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) +
                                                     ((size_t)bh * p.N + (size_t)tile * kTile) * 128);
+  uint4 u[8];
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int i = threadIdx.x + it * 256;  // 16 chunks of 8 values per row
+    u[it] = i < rows * 16 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+  }
   float amax = 0.f;
-  for (int i = threadIdx.x; i < rows * 16; i += 256) {  // 16 chunks of 8 values per row
-    const uint4 u = src[i];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const uint32_t w[4] = {u[it].x, u[it].y, u[it].z, u[it].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
@@ -63,63 +71,76 @@ __global__ void __launch_bounds__(256) v_amax_kernel(const QuantParams p) {
 }
 
 // One CTA per (bh, tile) and tensor (blockIdx.y): 0 = Q, 1 = K (rotated,
-// per-tile scale), 2 = V (per-head scale from vmax).  Lane l of a warp holds
-// coordinates 4l .. 4l+3 of its rows.
-__global__ void __launch_bounds__(256) quantize_kernel(const QuantParams p) {
+// per-tile scale), 2 = V (per-head scale from vmax).  Four lanes share a row:
+// lane l takes row 8 * warp + l / 4 and its coordinates 32 (l % 4) .. + 31.
+// The Walsh-Hadamard butterflies over index bits 0-4 run in registers, those
+// over bits 5 and 6 exchange with lanes l ^ 1 and l ^ 2.
+__global__ void __launch_bounds__(kQuantWarps * 32, 2) quantize_kernel(const QuantParams p) {
   const int tile = blockIdx.x % p.n_tiles, bh = blockIdx.x / p.n_tiles, which = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = lane & 3;
+  const int r = warp * 8 + (lane >> 2);
   const void* src_base = which == 0 ? p.q : which == 1 ? p.k : p.v;
   uint8_t* dst_base = which == 0 ? p.q8 : which == 1 ? p.k8 : p.v8;
   const size_t row0 = (size_t)bh * p.N + (size_t)tile * kTile;
   const int rows = min(kTile, p.N - tile * kTile);
-  float x[kQuantRowsPerWarp][4];
-  float amax = 0.f;
-  // (selected without indexing the parameter array, which would copy it to local memory)
-  const uint32_t sword = lane < 8 ? p.signs[0] : lane < 16 ? p.signs[1] : lane < 24 ? p.signs[2] : p.signs[3];
-  const uint32_t sbits = (sword >> ((lane & 7) * 4)) & 0xFu;
+  const bool live = r < rows;
+  float x[32];
+  {
+    uint4 u[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                  make_uint4(0u, 0u, 0u, 0u)};
+    if (live) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src_base) +
+                                                        (row0 + r) * 128 + quarter * 32);
 #pragma unroll
-  for (int i = 0; i < kQuantRowsPerWarp; ++i) {
-    const int r = warp * kQuantRowsPerWarp + i;
-    uint2 u = make_uint2(0u, 0u);
-    if (r < rows)
-      u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(src_base) + (row0 + r) * 128 + lane * 4);
-    x[i][0] = __uint_as_float(u.x << 16);
-    x[i][1] = __uint_as_float(u.x & 0xFFFF0000u);
-    x[i][2] = __uint_as_float(u.y << 16);
-    x[i][3] = __uint_as_float(u.y & 0xFFFF0000u);
-    if (which < 2) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if ((sbits >> c) & 1u) x[i][c] = -x[i][c];
-      // Walsh-Hadamard butterflies: index bits 0-1 inside the lane, bits
-      // 2-6 across lanes (partner lane = lane ^ 2^t)
-      float a0 = x[i][0] + x[i][1], a1 = x[i][0] - x[i][1];
-      float a2 = x[i][2] + x[i][3], a3 = x[i][2] - x[i][3];
-      x[i][0] = a0 + a2;
-      x[i][2] = a0 - a2;
-      x[i][1] = a1 + a3;
-      x[i][3] = a1 - a3;
-#pragma unroll
-      for (int t = 1; t < 32; t <<= 1) {
-        const bool upper = (lane & t) != 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float o = __shfl_xor_sync(0xffffffffu, x[i][c], t);
-          x[i][c] = upper ? o - x[i][c] : x[i][c] + o;
-        }
-      }
+      for (int c = 0; c < 4; ++c) u[c] = src[c];
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) amax = fmaxf(amax, fabsf(x[i][c]));
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[8 * c + 2 * j] = __uint_as_float(w[j] << 16);
+        x[8 * c + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
   }
-  __shared__ float red[8];
+  if (which < 2) {
+    // (selected without indexing the parameter array, which would copy it to local memory)
+    const uint32_t sw = quarter == 0 ? p.signs[0] : quarter == 1 ? p.signs[1] : quarter == 2 ? p.signs[2] : p.signs[3];
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if ((sw >> e) & 1u) x[e] = -x[e];
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if ((e & h) == 0) {
+          const float a = x[e], b = x[e + h];
+          x[e] = a + b;
+          x[e + h] = a - b;
+        }
+#pragma unroll
+    for (int t = 1; t < 4; t <<= 1) {
+      const bool upper = (lane & t) != 0;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, x[e], t);
+        x[e] = upper ? o - x[e] : x[e] + o;
+      }
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(x[e]));
+  __shared__ float red[kQuantWarps];
   if (which < 2) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     if (lane == 0) red[warp] = amax;
     __syncthreads();
     amax = red[0];
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    for (int i = 1; i < kQuantWarps; ++i) amax = fmaxf(amax, red[i]);
   } else {
     amax = __uint_as_float(p.vmax[bh]);
   }
@@ -131,12 +152,14 @@ __global__ void __launch_bounds__(256) quantize_kernel(const QuantParams p) {
     else if (which == 1) p.sk[(size_t)bh * p.n_tiles + tile] = sc;
     else if (tile == 0) p.sv[bh] = sc;
   }
+  if (live) {
+    uint32_t w[8];
 #pragma unroll
-  for (int i = 0; i < kQuantRowsPerWarp; ++i) {
-    const int r = warp * kQuantRowsPerWarp + i;
-    if (r < rows)
-      *reinterpret_cast<uint32_t*>(dst_base + (row0 + r) * 128 + lane * 4) =
-          pack_e4m3x4(x[i][0] * inv, x[i][1] * inv, x[i][2] * inv, x[i][3] * inv);
+    for (int j = 0; j < 8; ++j)
+      w[j] = pack_e4m3x4(x[4 * j] * inv, x[4 * j + 1] * inv, x[4 * j + 2] * inv, x[4 * j + 3] * inv);
+    uint4* dst = reinterpret_cast<uint4*>(dst_base + (row0 + r) * 128 + quarter * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -149,7 +172,7 @@ cudaError_t launch_fp8_quantize(const QuantParams& p, cudaStream_t s) {
   v_amax_kernel<<<blocks, 256, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  quantize_kernel<<<dim3(blocks, 3), 256, 0, s>>>(p);
+  quantize_kernel<<<dim3(blocks, 3), kQuantWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -437,6 +437,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// max(a, b, c) in one three-input instruction (sm_100 and later); a NaN
+// operand is ignored as in fmaxf.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Four FP32 values to e4m3 (round to nearest even, saturating at +-448),
 // packed with ``a`` in the lowest byte.  cvt...e4m3x2 puts its first source
 // operand in the upper byte of the pair.
