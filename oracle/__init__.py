@@ -19,6 +19,9 @@ merge       attention over a key range (split-KV partials) and the associative
 fp8         the e4m3 format, the Hadamard rotation of Q and K, power-of-two
             block scales, and the FP8 forward (online softmax with P
             rounded to e4m3) from quantised inputs.
+masks       attention under a sliding-window mask and a block mask (forward
+            and chain-rule backward), and the tile pairs such a mask leaves
+            visible.
 
 Every function is pinned by a CPU test against something other than itself
 (brute force, finite differences, closed forms, invariants, or the numbers
