@@ -48,6 +48,9 @@ _SIGS = {
     "attn_fp8_quantize_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
     "attn_fp8_quantize": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_masked": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
+    "attn_bwd_masked": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _I, _P,
+                             ctypes.c_size_t, _P]),
     "attn_profile_start": (_I, []),
     "attn_profile_stop": (_I, [_P]),
 }
@@ -186,6 +189,26 @@ def attn_fp8_quantize(q, k, v, signs, q8, k8, v8, sq, sk, sv, B, H, N, d, worksp
 def attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, B, H, N, d, causal, scale, stream=None, check=True) -> int:
     st = get_lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o), _ptr(lse), B, H,
                                 N, d, int(causal), float(scale), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_fwd_masked(q, k, v, o, lse, B, H, N, d_qk, d_v, window_left, window_right, block_mask, scale, stream=None,
+                    check=True) -> int:
+    st = get_lib().attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d_qk, d_v, int(window_left),
+                                   int(window_right), _ptr(block_mask), float(scale), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_bwd_masked(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, window_left, window_right, block_mask, scale,
+                    deterministic, workspace, workspace_bytes, stream=None, check=True) -> int:
+    st = get_lib().attn_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), B, H, N, d_qk, d_v, int(window_left), int(window_right), _ptr(block_mask),
+                                   float(scale), int(deterministic), _ptr(workspace), int(workspace_bytes),
+                                   _stream(stream))
     if check:
         _check(st)
     return st

@@ -519,9 +519,14 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d_qk, int d_v, int dete
   return workspace_layout(B, H, N, d_qk, deterministic).total;
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-             void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale,
-             int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// attn_bwd and attn_bwd_masked (mask != null: the masked one-CTA instances).
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+             void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale, int deterministic,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream, const attn::MaskSpec* mask) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (int st = check_common(B, H, N, scale, causal)) return st;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
@@ -541,7 +546,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (int st = make_map(&p.tm_v, v, BH, N, d_v)) return st;
   if (int st = make_map(&p.tm_do, dO, BH, N, d_v)) return st;
   // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)
-  p.pair_mode = (d_qk == 128 && cfg.bwd_pair) ? 1 : 0;
+  p.pair_mode = (d_qk == 128 && cfg.bwd_pair && mask == nullptr) ? 1 : 0;
+  if (mask != nullptr) p.mask = *mask;
   if (p.pair_mode) {
     if (int st = make_map(&p.tm_q_half, q, BH, N, d_qk, 64)) return st;
     if (int st = make_map(&p.tm_do_half, dO, BH, N, d_v, 64)) return st;
@@ -570,10 +576,94 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (prof)
     for (auto& ev : evs.ev)
       if (cudaEventCreate(&ev) != cudaSuccess) return ATTN_ERR_CUDA;
-  cudaError_t e = d_qk == 64 ? attn::launch_bwd_d64(p, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr)
-                             : attn::launch_bwd_d128(p, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr);
+  cudaError_t e;
+  if (mask != nullptr)
+    e = attn::launch_bwd_masked(p, d_qk, deterministic != 0, stream, prof ? &evs : nullptr);
+  else
+    e = d_qk == 64 ? attn::launch_bwd_d64(p, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr)
+                   : attn::launch_bwd_d128(p, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr);
   if (prof)
     for (int k = 0; k < 3; ++k) add_record(1 + k, evs.ev[k], evs.ev[k + 1]);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Mask of attn_fwd_masked / attn_bwd_masked from its arguments.
+int make_mask(attn::MaskSpec* m, int N, int window_left, int window_right, const unsigned char* block_mask) {
+  if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID_ARG;
+  m->left = window_left;
+  m->right = window_right;
+  m->block = block_mask;
+  m->n_tiles = (N + 127) / 128;
+  m->N = N;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale,
+             int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, causal, scale, deterministic, workspace,
+                  workspace_bytes, stream, nullptr);
+}
+
+int attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int window_left,
+                    int window_right, const unsigned char* block_mask, float scale, int deterministic,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  attn::MaskSpec m;
+  if (int st = check_common(B, H, N, scale, 0)) return st;
+  if (int st = make_mask(&m, N, window_left, window_right, block_mask)) return st;
+  if (block_mask != nullptr && !aligned16(block_mask)) return ATTN_ERR_MISALIGNED;
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, 0, scale, deterministic, workspace,
+                  workspace_bytes, stream, &m);
+}
+
+int attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d_qk,
+                    int d_v, int window_left, int window_right, const unsigned char* block_mask, float scale,
+                    cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (int st = check_common(B, H, N, scale, 0)) return st;
+  attn::FwdParams p;
+  memset(&p, 0, sizeof(p));
+  if (int st = make_mask(&p.mask, N, window_left, window_right, block_mask)) return st;
+  if (!bwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  if (block_mask != nullptr && !aligned16(block_mask)) return ATTN_ERR_MISALIGNED;
+  const Settings cfg = settings();
+  const int BH = B * H;
+  if (int st = make_map(&p.tm_q, q, BH, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_k, k, BH, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_v, v, BH, N, d_v)) return st;
+  if (int st = status_ptr(&p.status)) return st;
+  p.o = o;
+  p.lse = lse;
+  p.rescale_counter = cfg.rescale_counter;
+  p.timeout_ns = cfg.timeout_ns;
+  p.N = N;
+  p.BH = BH;
+  p.n_qtiles = (N + 127) / 128;
+  p.n_blocks = BH * p.n_qtiles;  // one query tile per CTA
+  p.max_ctas = cfg.fwd_max_ctas;
+  // persistent CTAs when units are short: short sequences, or a window that
+  // bounds every query tile to at most 32 key tiles
+  const bool short_window = window_left >= 0 && window_right >= 0 &&
+                            (long long)window_left + window_right <= 30ll * 128;
+  p.persist = cfg.fwd_persist >= 0 ? cfg.fwd_persist : ((N <= 4096 || short_window) ? 1 : 0);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.tau = cfg.tau;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  if (profiling()) {
+    if (cudaEventCreate(&ea) != cudaSuccess || cudaEventCreate(&eb) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaEventRecord(ea, stream);
+  }
+  const cudaError_t e = attn::launch_fwd_masked(p, d_qk, stream);
+  if (ea != nullptr) {
+    cudaEventRecord(eb, stream);
+    add_record(0, ea, eb);
+  }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -40,6 +40,7 @@
 
 #include <type_traits>
 
+#include "attn_mask.cuh"
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -195,9 +196,14 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(BwdParams p) {
 }
 
 // ---------------------------------------------------------------- main
-template <int D, bool CAUSAL, bool DETERMINISTIC>
+// MASK: pairs follow p.mask (window and block map; not with CAUSAL): each
+// key tile visits only the query tiles holding a visible pair, P is zeroed
+// per pair in tiles that are not fully visible, and in deterministic mode a
+// query tile takes its visible key tiles in ascending order.
+template <int D, bool CAUSAL, bool DETERMINISTIC, bool MASK = false>
 __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
+  static_assert(!(MASK && CAUSAL), "the masked instance expresses causality as a window");
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -223,8 +229,14 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     j = blockIdx.x - bh * n;
   }
   const int i_lo = CAUSAL ? j : 0;  // query tiles i_lo .. n-1, visited from n-1 down
-  const int n_it = n - i_lo;
-  auto tile_of = [&](int it) { return n - 1 - it; };
+  int n_it = n - i_lo;
+  if (MASK) {  // only the query tiles holding a visible pair with key tile j
+    n_it = 0;
+    for (int i = 0; i < n; ++i) n_it += mask_tile_visible(p.mask, i, j) ? 1 : 0;
+  }
+  // every role walks the same query tiles, from the last down
+  const int i_first = MASK ? mask_prev_query_tile(p.mask, j, n) : n - 1;
+  auto i_next = [&](int i) { return MASK ? mask_prev_query_tile(p.mask, j, i) : i - 1; };
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < L::kNumBars; ++b) {
@@ -262,12 +274,11 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         tma_load_3d(sbase + L::kVOff + c * kBSub, &p.tm_v, c * 64, j * kBTile, bh, bar(L::kBarKV));
       }
       int issued_q = 0, issued_do = 0;  // loads issued per ring
-      for (int it = 0; it < n_it; ++it) {
+      for (int it = 0, i = i_first; it < n_it; ++it, i = i_next(i)) {
         const int s = it % L::kQStages;
         const uint32_t ph = ((it / L::kQStages) & 1) ^ 1;
         const int sd = it % L::kDOStages;
         const uint32_t phd = ((it / L::kDOStages) & 1) ^ 1;
-        const int i = tile_of(it);
         if (!mbar_wait(bar(L::kBarQEmpty + s), ph, ctl, kBWhereProd)) break;
         mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kTileBytes + L::kVecBytes);
 #pragma unroll
@@ -433,16 +444,16 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     const float c_log2 = p.scale_log2;
     const bool key_dead = k_glob >= p.N;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = 0, i = i_first; it < n_it; ++it, i = i_next(i)) {
       const int s = it % L::kQStages;
-      const int i = tile_of(it);
       // LSE2 / D vectors arrive with Q_i on the stage's barrier
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + s), (it / L::kQStages) & 1, ctl, kBWhereEw + 3));
       if (!ok) break;
       const float* vec = reinterpret_cast<const float*>(smem + L::kVecOff + s * L::kVecBytes);
       const bool diag = CAUSAL && i == j;
       // the mask only bites on the diagonal tile and on a ragged last key tile
-      const bool mask_tile = diag || (j * kBTile + kBTile > p.N);
+      // (masked instance: on every tile the window does not cover whole)
+      const bool mask_tile = MASK ? !mask_tile_full(p.mask, i, j) : (diag || (j * kBTile + kBTile > p.N));
       // Phase 1 (needs S^T): P = 2^(S^T * scale * log2e - LSE2) for this
       // warpgroup's 64 queries, kept in FP32 registers and packed as bf16
       // P^T into columns 64h .. 64h+31 (inside the columns just read).
@@ -466,10 +477,21 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
           float p0 = ex2_mufu(x01.x), p1 = ex2_mufu(x01.y), p2 = ex2_mufu(x23.x), p3 = ex2_mufu(x23.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = i * kBTile + c0 + q;  // global query index of p0
-            if (key_dead || (diag && q0 < k_glob)) p0 = 0.f;
-            if (key_dead || (diag && q0 + 1 < k_glob)) p1 = 0.f;
-            if (key_dead || (diag && q0 + 2 < k_glob)) p2 = 0.f;
-            if (key_dead || (diag && q0 + 3 < k_glob)) p3 = 0.f;
+            if constexpr (MASK) {  // key k_glob is visible from query r when r - left <= k_glob <= r + right
+              auto hid = [&](int r) {
+                return key_dead || (p.mask.left >= 0 && k_glob < r - p.mask.left) ||
+                       (p.mask.right >= 0 && k_glob > r + p.mask.right);
+              };
+              if (hid(q0)) p0 = 0.f;
+              if (hid(q0 + 1)) p1 = 0.f;
+              if (hid(q0 + 2)) p2 = 0.f;
+              if (hid(q0 + 3)) p3 = 0.f;
+            } else {
+              if (key_dead || (diag && q0 < k_glob)) p0 = 0.f;
+              if (key_dead || (diag && q0 + 1 < k_glob)) p1 = 0.f;
+              if (key_dead || (diag && q0 + 2 < k_glob)) p2 = 0.f;
+              if (key_dead || (diag && q0 + 3 < k_glob)) p3 = 0.f;
+            }
           }
           pv[32 * m + q] = p0;
           pv[32 * m + q + 1] = p1;
@@ -537,8 +559,13 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
 #pragma unroll
       for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
         float a[32], b[32];
-        tmem_ld32(tmem + lane_base + L::kColDV + c0, a);
-        tmem_ld32(tmem + lane_base + L::kColDK + c0, b);
+        if (n_it > 0) {
+          tmem_ld32(tmem + lane_base + L::kColDV + c0, a);
+          tmem_ld32(tmem + lane_base + L::kColDK + c0, b);
+        } else {  // (masked instance) no query sees this key tile: dK = dV = 0
+#pragma unroll
+          for (int q = 0; q < 32; ++q) a[q] = b[q] = 0.f;
+        }
         uint32_t pa[16], pb[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -566,8 +593,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     const int tid = threadIdx.x - 384;
     const uint32_t tDQ = tmem + ((uint32_t)(quad * 32) << 16) + L::kColDQ;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int i = tile_of(it);
+    for (int it = 0, i = i_first; it < n_it; ++it, i = i_next(i)) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 9);
@@ -610,7 +636,13 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         if (tid == 0) {
           if (DETERMINISTIC && r == 0) {
             const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(ticket) != j) {  // tile i takes key tiles in ascending j
+            // tile i takes its (visible) key tiles in ascending order
+            int rank = j;
+            if (MASK) {
+              rank = 0;
+              for (int jj = 0; jj < j; ++jj) rank += mask_tile_visible(p.mask, i, jj) ? 1 : 0;
+            }
+            while (ld_acquire_gpu(ticket) != rank) {
               if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
                 if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
                 *ctl.abort = 1;
@@ -650,7 +682,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
 template <bool CAUSAL, bool DET>
 cudaError_t launch_bwd2_main(const BwdParams& p, cudaStream_t stream);
 
-template <int D, bool CAUSAL, bool DET>
+template <int D, bool CAUSAL, bool DET, bool MASK = false>
 cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const LaunchEvents* evs) {
   using L = BwdLayout<D>;
   auto mark = [&](int i) {
@@ -669,14 +701,14 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
   mark(1);
   bool paired = false;
   if constexpr (D == 128) {
-    if (p.pair_mode) {
+    if (p.pair_mode && !MASK) {
       cudaError_t e = launch_bwd2_main<CAUSAL, DET>(p, stream);
       if (e != cudaSuccess) return e;
       paired = true;
     }
   }
   if (!paired) {
-    auto kernel = bwd_kernel<D, CAUSAL, DET>;
+    auto kernel = bwd_kernel<D, CAUSAL, DET, MASK>;
     // setmaxnreg.inc waits for registers the dec released: the split must
     // match what the launch hands out
     cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, nullptr);

@@ -32,6 +32,7 @@
 // drained, tensor memory is released and the CTA exits.
 #pragma once
 
+#include "attn_mask.cuh"
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -108,11 +109,16 @@ enum : int {
 // p.sk and a per-head scale p.sv; the products run as kind::f8f6f4; the
 // softmax forms 2^8 P against a running max updated on every rise (the host
 // passes tau = 0) and stores it as e4m3 over the first 32 columns of S_t.
-template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool PERSIST, bool SPLIT = false, bool FP8 = false>
+// MASK (one query tile per CTA): keys follow p.mask (window and block map);
+// each unit visits only the key tiles holding a visible pair, in ascending
+// order, and masks per pair inside the tiles that are not fully visible.
+template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool PERSIST, bool SPLIT = false, bool FP8 = false,
+          bool MASK = false>
 __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<DQK, DV, NQT>::kMinBlocks)
     fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<DQK, DV, NQT, FP8 ? 1 : 2>;
   static_assert(!FP8 || (DQK == 128 && DV == 128 && !SPLIT), "FP8 instance: d = 128");
+  static_assert(!MASK || (NQT == 1 && !CAUSAL && !SPLIT && !FP8), "masked instance: one query tile, no other mode");
   // (the FP8 instance is built with POLY = 0: the polynomial share measured
   // slower there too, and its larger error moves more P codes)
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -164,6 +170,16 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     for (int t = 0; t < NQT; ++t) {
       const int qt = w.qblock * NQT + t;
       w.nkv[t] = qt < p.n_qtiles ? (CAUSAL ? qt + 1 : kv_len) : 0;
+      if (MASK && qt < p.n_qtiles) {  // visible key tiles; the first one in j0
+        int cnt = 0;
+        w.j0 = p.n_qtiles;
+        for (int kt = 0; kt < p.n_qtiles; ++kt)
+          if (mask_tile_visible(p.mask, qt, kt)) {
+            if (cnt == 0) w.j0 = kt;
+            ++cnt;
+          }
+        w.nkv[t] = cnt;
+      }
       w.nkv_max = w.nkv[t] > w.nkv_max ? w.nkv[t] : w.nkv_max;
     }
     return w;
@@ -232,7 +248,8 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
             tma_load_3d(sbase + t * L::kQBytes + c * kSubTile, &p.tm_q, c * L::kChunkElems,
                         (w.qblock * NQT + t) * kTile, w.bh, bar(L::kBarQFull));
         ++qn;
-        for (int j = 0; ok && j < w.nkv_max; ++j) {
+        int kt = w.j0;  // key tile of step j (masked instance: the visible ones in order)
+        for (int j = 0; ok && j < w.nkv_max; ++j, kt = MASK ? mask_next_key_tile(p.mask, w.qblock, kt) : kt + 1) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int ld = issued;
@@ -247,13 +264,13 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
 #pragma unroll
               for (int c = 0; c < L::kChunksQK; ++c)
-                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * L::kChunkElems, (w.j0 + j) * kTile, w.bh,
+                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * L::kChunkElems, kt * kTile, w.bh,
                             bar(L::kBarKVFull + s));
             } else {
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kVBytes);
 #pragma unroll
               for (int c = 0; c < L::kChunksV; ++c)
-                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * L::kChunkElems, (w.j0 + j) * kTile, w.bh,
+                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * L::kChunkElems, kt * kTile, w.bh,
                             bar(L::kBarKVFull + s));
             }
             issued = ld + 1;
@@ -455,16 +472,28 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     if (u >= n_units) continue;
     const Unit w = unit_at(u);
     const int n = w.nkv[t];
+    if constexpr (MASK) {
+      // a live tile whose rows see no key at all: O = 0, LSE = -inf
+      const int qt = w.qblock * NQT + t;
+      const int q_row = qt * kTile + quad * 32 + lane;
+      if (n == 0 && qt < p.n_qtiles && q_row < p.N) {
+        uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)w.bh * p.N + q_row) * DV);
+#pragma unroll
+        for (int c = 0; c < DV / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+        p.lse[(size_t)w.bh * p.N + q_row] = -INFINITY;
+      }
+    }
     if (n == 0) continue;
     const int bh = w.bh;
     const int qt = w.qblock * NQT + t;
     const int q_row = qt * kTile + quad * 32 + lane;
+    int kt = w.j0;  // key tile of step j
     float m = -INFINITY;  // running (possibly stale) max, log2 units
     float l = 0.f;        // running sum of 2^(s*c - m + kPOff)
     // FP8: the scores carry the query tile's and the key tile's scales
     const float c_q = FP8 ? p.scale_log2 * p.sq[(size_t)bh * p.n_qtiles + qt] : p.scale_log2;
-    for (int j = 0; j < n; ++j) {
-      const float c_log2 = FP8 ? c_q * p.sk[(size_t)bh * n_kv_tiles + w.j0 + j] : c_q;
+    for (int j = 0; j < n; ++j, kt = MASK ? mask_next_key_tile(p.mask, qt, kt) : kt + 1) {
+      const float c_log2 = FP8 ? c_q * p.sk[(size_t)bh * n_kv_tiles + kt] : c_q;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), cbit ^ (j & 1), ctl, kWhereSmS));
       if (!ok) break;
       if (quad == 0 && lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 9 + 2 * t);
@@ -478,8 +507,17 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       } else {
         tmem_ld128(tS, s);
       }
-      const int kbase = (w.j0 + j) * kTile;
-      if ((CAUSAL && j == qt) || kbase + kTile > n_keys) {
+      const int kbase = kt * kTile;
+      if constexpr (MASK) {
+        if (!mask_tile_full(p.mask, qt, kt)) {
+          // keys lo .. hi are visible from this row
+          const int lo = p.mask.left >= 0 ? q_row - p.mask.left : 0;
+          const int hi = p.mask.right >= 0 ? min(q_row + p.mask.right, p.N - 1) : p.N - 1;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (kbase + c < lo || kbase + c > hi) s[c] = -INFINITY;
+        }
+      } else if ((CAUSAL && j == qt) || kbase + kTile > n_keys) {
         const int lim = CAUSAL ? min(q_row + 1, p.N) : n_keys;  // keys < lim are visible
 #pragma unroll
         for (int c = 0; c < 128; ++c)
@@ -648,15 +686,15 @@ cudaError_t launch_fwd_split_instance(const FwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool FP8 = false>
+template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool FP8 = false, bool MASK = false>
 cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<DQK, DV, NQT, FP8 ? 1 : 2>;
   // Persistent CTAs pay off when units are short (few K/V tiles each); with
   // long units the one-unit-per-CTA kernel is leaner and the launch order
   // already balances.  p.max_ctas > 0 forces the persistent grid.
   const bool persist = p.max_ctas > 0 || p.persist;
-  auto kernel = persist ? fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, true, false, FP8>
-                        : fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, false, false, FP8>;
+  auto kernel = persist ? fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, true, false, FP8, MASK>
+                        : fwd_kernel<DQK, DV, NQT, CAUSAL, POLY, false, false, FP8, MASK>;
   // setmaxnreg.inc waits until the registers it asks for are free, so the
   // split must add up to what the launch actually hands out
   int sms = 0;

@@ -10,6 +10,17 @@ namespace attn {
 
 struct DeviceStatus;
 
+// Mask of the masked forward / backward (attn_fwd_masked, attn_bwd_masked):
+// query i sees key j when i - left <= j <= i + right (left / right < 0:
+// unbounded), j < N, and block[i / 128 * n_tiles + j / 128] != 0 (block may
+// be null: all ones).
+struct MaskSpec {
+  int left, right;
+  const uint8_t* block;  // device [n_tiles, n_tiles] or null
+  int n_tiles;
+  int N;
+};
+
 struct FwdParams {
   CUtensorMap tm_q;  // [BH, N, d_qk] bf16, box 64 x 128 x 1, 128-byte swizzle
   CUtensorMap tm_k;  // [BH, N, d_qk]
@@ -40,6 +51,7 @@ struct FwdParams {
   const float* sk;
   const float* sv;
   float p_off;  // FP8: P is stored as e4m3(2^p_off P), p_off = 8 - tau
+  MaskSpec mask;  // masked instances only
   float scale_log2;  // scale * log2(e)
   float tau;         // rescale threshold, log2 units
 };
@@ -70,6 +82,7 @@ struct BwdParams {
   float scale;
   float scale_log2;
   int pair_mode;  // 1: CTA-pair main kernel (d = 128) and its accumulator layout
+  MaskSpec mask;  // masked instances only
 };
 
 // Optional events recorded on the launch stream around each backward kernel:
@@ -95,6 +108,10 @@ cudaError_t launch_fwd_split(const FwdParams& p, int d_qk, int nqt, cudaStream_t
 // FP8 forward (d = 128, two query tiles per CTA) and the quantiser that
 // prepares its inputs (attn_fp8.cu).
 cudaError_t launch_fwd_fp8(const FwdParams& p, bool causal, cudaStream_t s);
+
+// Masked forward / backward (p.mask), d = 64 or 128 (attn_masked.cu).
+cudaError_t launch_fwd_masked(const FwdParams& p, int d, cudaStream_t s);
+cudaError_t launch_bwd_masked(const BwdParams& p, int d, bool deterministic, cudaStream_t s, const LaunchEvents* ev);
 struct QuantParams {
   const void* q;
   const void* k;

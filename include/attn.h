@@ -100,6 +100,33 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Masked attention ("Attention at Scale -- From FlashAttention to
+ * FlashAttention-4", FlexAttention section: variants such as sliding windows
+ * as a boolean mask over (query, key) pairs, plus a precomputed block map
+ * whose empty blocks the kernel skips).  Query i sees key j when
+ *     i - window_left <= j <= i + window_right     (-1: unbounded on that side)
+ * and block_mask[(i / 128) * T + j / 128] != 0, T = ceil(N / 128).
+ *   window_left, window_right   >= -1 (left = -1, right = 0 is the causal mask)
+ *   block_mask   device uint8 [T, T], 16-byte aligned, shared by every (b, h),
+ *                or NULL (all tiles allowed)
+ * Only the tile pairs holding a visible pair are computed; pairs are masked
+ * individually inside tiles the window does not cover whole.  A query row
+ * with no visible key gets O = 0 and LSE = -inf (and zero dQ).  Other
+ * arguments, layouts and the backward workspace are those of attn_fwd /
+ * attn_bwd; d_qk = d_v = 64 or 128.  The forward runs one 128-row query tile
+ * per CTA; the backward uses the one-CTA kernel (attn_set_bwd_pair does not
+ * apply).  Returns ATTN_OK or an argument / launch error.
+ */
+int attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d_qk,
+                    int d_v, int window_left, int window_right, const unsigned char* block_mask, float scale,
+                    cudaStream_t stream);
+
+int attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int window_left,
+                    int window_right, const unsigned char* block_mask, float scale, int deterministic,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Split-KV forward ("Attention at Scale -- From FlashAttention to
  * FlashAttention-4": the FlashInfer section's associative merge of attention
  * over disjoint key sets, and the "Sequence-Aware Split Heuristic" section's

@@ -214,3 +214,22 @@ def test_fp8_argument_errors(lib):
     assert f(p, p, p, p, p, p, p, p, 1, 2, 300, 64, 0, 0.1, None) == A.ATTN_ERR_UNSUPPORTED
     assert f(p, 0x1001, p, p, p, p, p, p, 1, 2, 300, 128, 0, 0.1, None) == A.ATTN_ERR_MISALIGNED
     assert f(p, p, p, p, p, p, p, p, 1, 2, 300, 128, 2, 0.1, None) == A.ATTN_ERR_INVALID_ARG
+
+
+def test_masked_argument_errors(lib):
+    A = lib
+    L = lib.get_lib()
+    p = 0x1000
+    f = L.attn_fwd_masked
+    assert f(p, p, p, p, p, 1, 2, 300, 128, 128, -2, 0, None, 0.1, None) == A.ATTN_ERR_INVALID_ARG
+    assert f(p, p, p, p, p, 1, 2, 300, 128, 128, 5, -3, None, 0.1, None) == A.ATTN_ERR_INVALID_ARG
+    assert f(p, p, p, p, p, 1, 2, 300, 192, 128, -1, 0, None, 0.1, None) == A.ATTN_ERR_UNSUPPORTED
+    assert f(p, p, p, p, p, 1, 2, 300, 128, 128, -1, 0, 0x1003, 0.1, None) == A.ATTN_ERR_MISALIGNED
+    assert f(0, p, p, p, p, 1, 2, 300, 128, 128, -1, 0, None, 0.1, None) == A.ATTN_ERR_INVALID_ARG
+    assert f(p, p, p, p, p, 1, 2, 300, 128, 128, -1, 0, None, -0.1, None) == A.ATTN_ERR_INVALID_ARG
+    b = L.attn_bwd_masked
+    ws = A.attn_bwd_workspace_bytes(1, 2, 300, 64, 64, 0)
+    assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, -2, 0, None, 0.1, 0, p, ws, None) == A.ATTN_ERR_INVALID_ARG
+    assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, None, 0.1, 0, p, ws - 1, None) == A.ATTN_ERR_WORKSPACE
+    assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, 0x1001, 0.1, 0, p, ws, None) == A.ATTN_ERR_MISALIGNED
+    assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, None, 0.1, 2, p, ws, None) == A.ATTN_ERR_INVALID_ARG
