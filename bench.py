@@ -14,7 +14,15 @@ fraction of the measured dense BF16 peak.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the FP64 CPU oracle on the host cores (a bounded sample
-of the same workload per step).  Under torchrun every rank runs the same
+of the same workload per step).
+
+  python bench.py --case fp8|splitkv|masked [--B --H --N ...]
+
+times one of the library's other paths instead (one GPU; a JSON line with its
+own fields; no contract line): the FP8 quantiser + FP8 forward, the split-KV
+decode forward (--Nq queries against --Nk keys, the heuristic's ranges), or
+the masked forward + backward (--window-left / --window-right, --block-density
+for a seeded random block map).  Under torchrun every rank runs the same
 workload on its own GPU (independent replicas: no data exchange), timing is
 bracketed by barriers and the slowest rank's time is used.
 """
@@ -407,6 +415,108 @@ def run_reference(args, world, rank):
     print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------- other library paths
+def run_case(args):
+    """Time the FP8, split-KV or masked path (CUDA events, L2 flushed before
+    each timed call, median of --steps after --warmup)."""
+    import numpy as np
+    import torch
+
+    import exact_attention_77_gb300 as A
+    import synth
+
+    A.get_lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    B, H, N, d = args.B, args.H, args.N, args.d
+    scale = 1.0 / math.sqrt(d)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    out = {"case": args.case, "steps": args.steps, "warmup": args.warmup, "data": "synthetic (seeded N(0,1) bf16)"}
+    if args.case == "fp8":
+        t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, d, d), seed=0, with_do=False, device=dev)
+        nt = (N + 127) // 128
+        q8, k8, v8 = (torch.empty((B, H, N, d), dtype=torch.uint8, device=dev) for _ in range(3))
+        sq, sk = torch.empty((B, H, nt), device=dev), torch.empty((B, H, nt), device=dev)
+        sv = torch.empty((B, H), device=dev)
+        nb = A.attn_fp8_quantize_workspace_bytes(B, H)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        signs = [1 if (i * 2654435761) & 0x100 else -1 for i in range(d)]
+        quant = lambda: A.attn_fp8_quantize(t["q"], t["k"], t["v"], signs, q8, k8, v8, sq, sk, sv, B, H, N, d, ws, nb)
+        fwd = lambda: A.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, B, H, N, d, args.causal, scale)
+        mq = timed(quant)
+        mf = timed(fwd)
+        fl = flops_fwd(args)
+        out.update({"config": {"B": B, "H": H, "N": N, "d": d, "causal": bool(args.causal)}, "quantize_ms": mq,
+                    "forward_ms": mf, "forward_tflops": fl / mf / 1e9, "end_to_end_tflops": fl / (mq + mf) / 1e9})
+    elif args.case == "splitkv":
+        t = synth.decode_inputs_torch(synth.DecodeShape(B, H, args.Nq, args.Nk, d, d), seed=0, device=dev)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        ns = A.attn_splitkv_heuristic(B, H, args.Nq, args.Nk, d, sms)
+        nb = A.attn_fwd_splitkv_workspace_bytes(B, H, args.Nq, args.Nk, d, ns)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        o = torch.empty((B, H, args.Nq, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, args.Nq), dtype=torch.float32, device=dev)
+        fn = lambda: A.attn_fwd_splitkv(t["q"], t["k"], t["v"], o, lse, B, H, args.Nq, args.Nk, d, d, scale, ns, ws, nb)
+        ms = timed(fn)
+        byts = B * H * (2 * args.Nk + 2 * args.Nq) * d * 2
+        out.update({"config": {"B": B, "H": H, "N_q": args.Nq, "N_k": args.Nk, "d": d, "ranges": ns}, "ms": ms,
+                    "gbs": byts / ms / 1e6, "note": "one call (split forward + merge), bytes = K, V, Q, O"})
+    else:
+        t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, d, d), seed=0, device=dev)
+        T = (N + 127) // 128
+        block = None
+        if args.block_density < 1.0:
+            rng = np.random.Generator(np.random.PCG64(0))
+            block = torch.from_numpy((rng.random((T, T)) < args.block_density).astype(np.uint8)).to(dev)
+        o = torch.empty_like(t["v"])
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+        nb = A.attn_bwd_workspace_bytes(B, H, N, d, d, args.det)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        wl, wr = args.window_left, args.window_right
+        fwd = lambda: A.attn_fwd_masked(t["q"], t["k"], t["v"], o, lse, B, H, N, d, d, wl, wr, block, scale)
+        bwd = lambda: A.attn_bwd_masked(t["q"], t["k"], t["v"], o, t["do"], lse, dq, dk, dv, B, H, N, d, d, wl, wr,
+                                        block, scale, args.det, ws, nb)
+        mf = timed(fwd)
+        fwd()
+        mb = timed(bwd)
+        # visible pairs from the window per row, times the kept share of tiles when a block map is used
+        i = np.arange(N)
+        lo = np.maximum(0, i - wl) if wl >= 0 else np.zeros(N, np.int64)
+        hi = np.minimum(N - 1, i + wr) if wr >= 0 else np.full(N, N - 1)
+        pairs = float((hi - lo + 1).clip(min=0).sum())
+        if block is not None:
+            pairs *= float(block.float().mean())
+        fl = 4.0 * B * H * d * pairs
+        out.update({"config": {"B": B, "H": H, "N": N, "d": d, "window": [wl, wr], "block_density": args.block_density,
+                               "dq_mode": "deterministic" if args.det else "atomic"},
+                    "forward_ms": mf, "backward_ms": mb, "forward_tflops": fl / mf / 1e9,
+                    "backward_tflops": 2.5 * fl / mb / 1e9,
+                    "note": "TFLOP/s over the visible pairs (with a block map: window pairs x kept share of tiles)"})
+    st, where = A.attn_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status: {A.status_string(st)} at {where}")
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,8 +532,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="head groups pipelined through host copies and compute in the e2e leg")
+    ap.add_argument("--case", choices=("step", "fp8", "splitkv", "masked"), default="step",
+                    help="step: the benchmark contract; others time the library's other paths")
+    ap.add_argument("--Nq", type=int, default=1)
+    ap.add_argument("--Nk", type=int, default=16384)
+    ap.add_argument("--window-left", type=int, default=-1)
+    ap.add_argument("--window-right", type=int, default=0)
+    ap.add_argument("--block-density", type=float, default=1.0)
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.case != "step":
+        run_case(args)
+        return
     world, rank, local = dist_env()
     if world != args.gpus and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
