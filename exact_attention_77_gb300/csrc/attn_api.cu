@@ -139,8 +139,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_common(int B, int H, int N, float scale, int causal) {
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if ((long long)B * H >= (1ll << 31) || N >= (1 << 24)) return ATTN_ERR_INVALID_ARG;
-  // the running max is taken as max(S) * scale: the scale must not be negative
-  if (!isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  // the running max is taken as max(S) * scale, and hidden scores are -inf
+  // before the scale is applied: the scale must be positive
+  if (!isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
@@ -363,7 +364,7 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (int st = check_split(B, H, N_q, N_k, n_splits)) return st;
-  if (!isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (!isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (!fwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
   const int BH = B * H;

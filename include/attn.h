@@ -66,7 +66,7 @@ typedef enum {
  *   lse [B,H,N]    fp32, written: natural-log log-sum-exp of the scaled,
  *                  unmasked scores of each query row (what the backward needs)
  *   causal         0 or 1 (top-left aligned: query i sees keys 0..i)
- *   scale          finite and >= 0; usually 1/sqrt(d_qk)
+ *   scale          finite and > 0; usually 1/sqrt(d_qk)
  * Returns ATTN_OK or an argument / launch error (see the enum).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d_qk,

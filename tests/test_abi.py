@@ -85,7 +85,7 @@ def test_forward_argument_errors(lib):
     assert _fwd(lib, scale=float("nan")) == A.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, scale=float("inf")) == A.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, scale=-0.125) == A.ATTN_ERR_INVALID_ARG
-    assert _fwd(lib, scale=0.0, q=0) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0) == A.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, dqk=96, dv=96) == A.ATTN_ERR_UNSUPPORTED
     assert _fwd(lib, dqk=128, dv=64) == A.ATTN_ERR_UNSUPPORTED
     assert _fwd(lib, k=0x1008) == A.ATTN_ERR_MISALIGNED
