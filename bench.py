@@ -467,18 +467,22 @@ def run_case(args):
         out.update({"config": {"B": B, "H": H, "N": N, "d": d, "causal": bool(args.causal)}, "quantize_ms": mq,
                     "forward_ms": mf, "forward_tflops": fl / mf / 1e9, "end_to_end_tflops": fl / (mq + mf) / 1e9})
     elif args.case == "splitkv":
-        t = synth.decode_inputs_torch(synth.DecodeShape(B, H, args.Nq, args.Nk, d, d), seed=0, device=dev)
+        Hkv = args.Hkv if args.Hkv > 0 else H
+        tq = synth.decode_inputs_torch(synth.DecodeShape(B, H, args.Nq, 1, d, d), seed=0, device=dev)
+        tk = synth.decode_inputs_torch(synth.DecodeShape(B, Hkv, 1, args.Nk, d, d), seed=1, device=dev)
+        rows = (H // Hkv) * args.Nq  # query rows per K/V head (grouped-query heads packed)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        ns = A.attn_splitkv_heuristic(B, H, args.Nq, args.Nk, d, sms)
-        nb = A.attn_fwd_splitkv_workspace_bytes(B, H, args.Nq, args.Nk, d, ns)
+        ns = A.attn_splitkv_heuristic(B, Hkv, rows, args.Nk, d, sms)
+        nb = A.attn_fwd_splitkv_workspace_bytes(B, Hkv, rows, args.Nk, d, ns)
         ws = torch.empty(nb, dtype=torch.uint8, device=dev)
         o = torch.empty((B, H, args.Nq, d), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, H, args.Nq), dtype=torch.float32, device=dev)
-        fn = lambda: A.attn_fwd_splitkv(t["q"], t["k"], t["v"], o, lse, B, H, args.Nq, args.Nk, d, d, scale, ns, ws, nb)
+        fn = lambda: A.attn_fwd_splitkv_gqa(tq["q"], tk["k"], tk["v"], o, lse, B, H, Hkv, args.Nq, args.Nk, d, d, scale,
+                                            ns, ws, nb)
         ms = timed(fn)
-        byts = B * H * (2 * args.Nk + 2 * args.Nq) * d * 2
-        out.update({"config": {"B": B, "H": H, "N_q": args.Nq, "N_k": args.Nk, "d": d, "ranges": ns}, "ms": ms,
-                    "gbs": byts / ms / 1e6, "note": "one call (split forward + merge), bytes = K, V, Q, O"})
+        byts = B * (2 * Hkv * args.Nk + 2 * H * args.Nq) * d * 2
+        out.update({"config": {"B": B, "H": H, "H_kv": Hkv, "N_q": args.Nq, "N_k": args.Nk, "d": d, "ranges": ns},
+                    "ms": ms, "gbs": byts / ms / 1e6, "note": "one call (split forward + merge), bytes = K, V, Q, O"})
     else:
         t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, d, d), seed=0, device=dev)
         T = (N + 127) // 128
@@ -536,6 +540,7 @@ def main(argv=None):
                     help="step: the benchmark contract; others time the library's other paths")
     ap.add_argument("--Nq", type=int, default=1)
     ap.add_argument("--Nk", type=int, default=16384)
+    ap.add_argument("--Hkv", type=int, default=0, help="splitkv case: K/V heads (grouped-query; 0 = --H)")
     ap.add_argument("--window-left", type=int, default=-1)
     ap.add_argument("--window-right", type=int, default=0)
     ap.add_argument("--block-density", type=float, default=1.0)

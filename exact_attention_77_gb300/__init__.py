@@ -51,6 +51,8 @@ _SIGS = {
     "attn_fwd_masked": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
     "attn_bwd_masked": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _I, _P,
                              ctypes.c_size_t, _P]),
+    "attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_splitkv_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t, _P]),
     "attn_profile_start": (_I, []),
     "attn_profile_stop": (_I, [_P]),
 }
@@ -209,6 +211,24 @@ def attn_bwd_masked(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, window_
                                    _ptr(dv), B, H, N, d_qk, d_v, int(window_left), int(window_right), _ptr(block_mask),
                                    float(scale), int(deterministic), _ptr(workspace), int(workspace_bytes),
                                    _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d_qk, d_v, causal, scale, stream=None, check=True) -> int:
+    st = get_lib().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N, d_qk, d_v, int(causal),
+                                float(scale), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_fwd_splitkv_gqa(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d_qk, d_v, scale, n_splits, workspace,
+                         workspace_bytes, stream=None, check=True) -> int:
+    st = get_lib().attn_fwd_splitkv_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N_q, N_k, d_qk,
+                                        d_v, float(scale), int(n_splits), _ptr(workspace), int(workspace_bytes),
+                                        _stream(stream))
     if check:
         _check(st)
     return st

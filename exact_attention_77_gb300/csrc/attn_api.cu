@@ -292,8 +292,14 @@ int attn_set_rescale_threshold(float tau) {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d_qk,
              int d_v, int causal, float scale, cudaStream_t stream) {
+  return attn_fwd_gqa(q, k, v, o, lse, B, H, H, N, d_qk, d_v, causal, scale, stream);
+}
+
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                 int d_qk, int d_v, int causal, float scale, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (int st = check_common(B, H, N, scale, causal)) return st;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (!fwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
   const Settings cfg = settings();
@@ -301,8 +307,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   memset(&p, 0, sizeof(p));
   const int BH = B * H;
   if (int st = make_map(&p.tm_q, q, BH, N, d_qk)) return st;
-  if (int st = make_map(&p.tm_k, k, BH, N, d_qk)) return st;
-  if (int st = make_map(&p.tm_v, v, BH, N, d_v)) return st;
+  if (int st = make_map(&p.tm_k, k, B * H_kv, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_v, v, B * H_kv, N, d_v)) return st;
   if (int st = status_ptr(&p.status)) return st;
   p.o = o;
   p.lse = lse;
@@ -310,6 +316,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.timeout_ns = cfg.timeout_ns;
   p.N = N;
   p.BH = BH;
+  p.h_q = H;
+  p.kv_group = H / H_kv;
   p.n_qtiles = (N + 127) / 128;
   const int nqt = d_qk == 192 ? 2 : cfg.fwd_tiles;
   p.n_blocks = BH * ((p.n_qtiles + nqt - 1) / nqt);
@@ -501,6 +509,18 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* sq
     add_record(0, ea, eb);
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+                         int N_q, int N_k, int d_qk, int d_v, float scale, int n_splits, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  if (H < 1 || H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  const long long rows = (long long)(H / H_kv) * N_q;
+  if (N_q < 1 || rows >= (1 << 24)) return ATTN_ERR_INVALID_ARG;
+  // the H / H_kv query heads of one K/V head are contiguous in [B, H, N_q, d]:
+  // as split-KV over B * H_kv heads of (H / H_kv) * N_q query rows
+  return attn_fwd_splitkv(q, k, v, o, lse, B, H_kv, (int)rows, N_k, d_qk, d_v, scale, n_splits, workspace,
+                          workspace_bytes, stream);
 }
 
 int attn_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o, float* lse, int BH, int N,

@@ -248,6 +248,9 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
             tma_load_3d(sbase + t * L::kQBytes + c * kSubTile, &p.tm_q, c * L::kChunkElems,
                         (w.qblock * NQT + t) * kTile, w.bh, bar(L::kBarQFull));
         ++qn;
+        // K/V head of this unit (grouped-query attention shares one among kv_group query heads)
+        const int kv_bh =
+            p.kv_group <= 1 ? w.bh : (w.bh / p.h_q) * (p.h_q / p.kv_group) + (w.bh % p.h_q) / p.kv_group;
         int kt = w.j0;  // key tile of step j (masked instance: the visible ones in order)
         for (int j = 0; ok && j < w.nkv_max; ++j, kt = MASK ? mask_next_key_tile(p.mask, w.qblock, kt) : kt + 1) {
 #pragma unroll
@@ -264,13 +267,13 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
 #pragma unroll
               for (int c = 0; c < L::kChunksQK; ++c)
-                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * L::kChunkElems, kt * kTile, w.bh,
+                tma_load_3d(dst + c * kSubTile, &p.tm_k, c * L::kChunkElems, kt * kTile, kv_bh,
                             bar(L::kBarKVFull + s));
             } else {
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kVBytes);
 #pragma unroll
               for (int c = 0; c < L::kChunksV; ++c)
-                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * L::kChunkElems, kt * kTile, w.bh,
+                tma_load_3d(dst + c * kSubTile, &p.tm_v, c * L::kChunkElems, kt * kTile, kv_bh,
                             bar(L::kBarKVFull + s));
             }
             issued = ld + 1;

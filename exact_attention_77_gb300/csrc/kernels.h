@@ -52,6 +52,11 @@ struct FwdParams {
   const float* sv;
   float p_off;  // FP8: P is stored as e4m3(2^p_off P), p_off = 8 - tau
   MaskSpec mask;  // masked instances only
+  // grouped-query attention: unit (b, h) reads K/V head b * h_kv + h / kv_group
+  // (h < h_q query heads, h_kv = h_q / kv_group); kv_group = 1: one K/V head
+  // per query head
+  int h_q;
+  int kv_group;
   float scale_log2;  // scale * log2(e)
   float tau;         // rescale threshold, log2 units
 };

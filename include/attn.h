@@ -73,6 +73,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int d_v, int causal, float scale, cudaStream_t stream);
 
 /*
+ * Forward with grouped-query attention (the K/V-head sharing that "Attention
+ * at Scale -- From FlashAttention to FlashAttention-4", section
+ * "Sequence-Aware Split Heuristic", names as GQA/MQA): H query heads share
+ * H_kv K/V heads, query head h reading K/V head h / (H / H_kv).
+ *   q, o [B,H,N,d], lse [B,H,N]; k, v [B,H_kv,N,d]; H % H_kv == 0 (H_kv = H
+ *   is attn_fwd, H_kv = 1 multi-query attention).  Other arguments as attn_fwd.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                 int d_qk, int d_v, int causal, float scale, cudaStream_t stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for these sizes (0 for sizes the
  * backward does not accept).  The workspace holds, per (b, h): the FP32 row
  * terms D_i = dO_i . O_i and LSE_i * log2(e) (padded to a multiple of 128
@@ -153,6 +164,21 @@ int attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, 
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
                      int N_k, int d_qk, int d_v, float scale, int n_splits, void* workspace, size_t workspace_bytes,
                      cudaStream_t stream);
+
+/*
+ * Split-KV forward with grouped-query attention (decode with few K/V heads,
+ * the case the sequence-aware split section describes): q, o [B,H,N_q,d],
+ * lse [B,H,N_q], k, v [B,H_kv,N_k,d], H % H_kv == 0.  The H / H_kv query heads
+ * of one K/V head are contiguous rows of q, so this is exactly
+ * attn_fwd_splitkv over B * H_kv heads of (H / H_kv) * N_q query rows (each
+ * K/V tile is read once per group, not once per query head): size the
+ * workspace with attn_fwd_splitkv_workspace_bytes(B, H_kv, (H / H_kv) * N_q,
+ * N_k, d_v, n_splits) and choose n_splits with attn_splitkv_heuristic(B,
+ * H_kv, (H / H_kv) * N_q, N_k, d_qk, n_sms).
+ */
+int attn_fwd_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+                         int N_q, int N_k, int d_qk, int d_v, float scale, int n_splits, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Workspace bytes attn_fwd_splitkv needs for these sizes and this requested

@@ -233,3 +233,17 @@ def test_masked_argument_errors(lib):
     assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, None, 0.1, 0, p, ws - 1, None) == A.ATTN_ERR_WORKSPACE
     assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, 0x1001, 0.1, 0, p, ws, None) == A.ATTN_ERR_MISALIGNED
     assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, None, 0.1, 2, p, ws, None) == A.ATTN_ERR_INVALID_ARG
+
+
+def test_gqa_argument_errors(lib):
+    A = lib
+    L = lib.get_lib()
+    p = 0x1000
+    assert L.attn_fwd_gqa(p, p, p, p, p, 1, 8, 3, 256, 128, 128, 0, 0.1, None) == A.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_gqa(p, p, p, p, p, 1, 8, 0, 256, 128, 128, 0, 0.1, None) == A.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_gqa(p, p, p, p, p, 1, 8, 2, 256, 96, 96, 0, 0.1, None) == A.ATTN_ERR_UNSUPPORTED
+    f = L.attn_fwd_splitkv_gqa
+    ws = A.attn_fwd_splitkv_workspace_bytes(1, 2, 4, 1000, 128, 2)
+    assert f(p, p, p, p, p, 1, 8, 3, 1, 1000, 128, 128, 0.1, 2, p, ws, None) == A.ATTN_ERR_INVALID_ARG
+    assert f(p, p, p, p, p, 1, 8, 2, 0, 1000, 128, 128, 0.1, 2, p, ws, None) == A.ATTN_ERR_INVALID_ARG
+    assert f(p, p, p, p, p, 1, 8, 2, 1, 1000, 128, 128, 0.1, 2, p, ws - 1, None) == A.ATTN_ERR_WORKSPACE
