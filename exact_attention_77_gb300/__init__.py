@@ -53,6 +53,8 @@ _SIGS = {
                              ctypes.c_size_t, _P]),
     "attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_splitkv_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t,
+                          _P]),
     "attn_profile_start": (_I, []),
     "attn_profile_stop": (_I, [_P]),
 }
@@ -229,6 +231,16 @@ def attn_fwd_splitkv_gqa(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d_qk, d_v, scale
     st = get_lib().attn_fwd_splitkv_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N_q, N_k, d_qk,
                                         d_v, float(scale), int(n_splits), _ptr(workspace), int(workspace_bytes),
                                         _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def attn_bwd_gqa(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d_qk, d_v, causal, scale, deterministic, workspace,
+                 workspace_bytes, stream=None, check=True) -> int:
+    st = get_lib().attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                                B, H, H_kv, N, d_qk, d_v, int(causal), float(scale), int(deterministic),
+                                _ptr(workspace), int(workspace_bytes), _stream(stream))
     if check:
         _check(st)
     return st

@@ -548,9 +548,11 @@ namespace {
 
 // attn_bwd and attn_bwd_masked (mask != null: the masked one-CTA instances).
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
-             void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale, int deterministic,
-             void* workspace, size_t workspace_bytes, cudaStream_t stream, const attn::MaskSpec* mask) {
+             void* dk, void* dv, int B, int H, int H_kv, int N, int d_qk, int d_v, int causal, float scale,
+             int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+             const attn::MaskSpec* mask) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (H_kv < 1 || H_kv > H || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (int st = check_common(B, H, N, scale, causal)) return st;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
   if (!bwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
@@ -564,12 +566,15 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   attn::BwdParams p;
   memset(&p, 0, sizeof(p));
   const int BH = B * H;
+  const bool gqa = H_kv < H;
   if (int st = make_map(&p.tm_q, q, BH, N, d_qk)) return st;
-  if (int st = make_map(&p.tm_k, k, BH, N, d_qk)) return st;
-  if (int st = make_map(&p.tm_v, v, BH, N, d_v)) return st;
+  if (int st = make_map(&p.tm_k, k, B * H_kv, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_v, v, B * H_kv, N, d_v)) return st;
   if (int st = make_map(&p.tm_do, dO, BH, N, d_v)) return st;
+  p.h_q = H;
+  p.kv_group = H / H_kv;
   // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)
-  p.pair_mode = (d_qk == 128 && cfg.bwd_pair && mask == nullptr) ? 1 : 0;
+  p.pair_mode = (d_qk == 128 && cfg.bwd_pair && mask == nullptr && !gqa) ? 1 : 0;
   if (mask != nullptr) p.mask = *mask;
   if (p.pair_mode) {
     if (int st = make_map(&p.tm_q_half, q, BH, N, d_qk, 64)) return st;
@@ -602,6 +607,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   cudaError_t e;
   if (mask != nullptr)
     e = attn::launch_bwd_masked(p, d_qk, deterministic != 0, stream, prof ? &evs : nullptr);
+  else if (gqa)
+    e = attn::launch_bwd_gqa(p, d_qk, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr);
   else
     e = d_qk == 64 ? attn::launch_bwd_d64(p, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr)
                    : attn::launch_bwd_d128(p, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr);
@@ -628,7 +635,14 @@ extern "C" {
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
              void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale,
              int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, causal, scale, deterministic, workspace,
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d_qk, d_v, causal, scale, deterministic, workspace,
+                  workspace_bytes, stream, nullptr);
+}
+
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d_qk, int d_v, int causal,
+                 float scale, int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d_qk, d_v, causal, scale, deterministic, workspace,
                   workspace_bytes, stream, nullptr);
 }
 
@@ -640,7 +654,7 @@ int attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, 
   if (int st = check_common(B, H, N, scale, 0)) return st;
   if (int st = make_mask(&m, N, window_left, window_right, block_mask)) return st;
   if (block_mask != nullptr && !aligned16(block_mask)) return ATTN_ERR_MISALIGNED;
-  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, 0, scale, deterministic, workspace,
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d_qk, d_v, 0, scale, deterministic, workspace,
                   workspace_bytes, stream, &m);
 }
 

@@ -200,10 +200,14 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(BwdParams p) {
 // key tile visits only the query tiles holding a visible pair, P is zeroed
 // per pair in tiles that are not fully visible, and in deterministic mode a
 // query tile takes its visible key tiles in ascending order.
-template <int D, bool CAUSAL, bool DETERMINISTIC, bool MASK = false>
+// GQA: bh indexes K/V heads (p.kv_group query heads share one); each key tile
+// walks the query tiles of all its query heads, so dK and dV sum over them
+// in tensor memory, while dQ and the tickets stay per query head.
+template <int D, bool CAUSAL, bool DETERMINISTIC, bool MASK = false, bool GQA = false>
 __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
   static_assert(!(MASK && CAUSAL), "the masked instance expresses causality as a window");
+  static_assert(!(MASK && GQA), "the masked instance has one K/V head per query head");
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -220,23 +224,38 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
   // work unit: key tile j of head bh.  Causal key tiles with small j are the
   // longest (they see the most query tiles) and go first in either order.
   const int n = p.n_tiles;
+  const int n_heads = GQA ? p.BH / p.kv_group : p.BH;  // K/V heads
   int j, bh;
   if (DETERMINISTIC) {  // key-tile-major: a CTA waits only on CTAs launched before it
-    j = blockIdx.x / p.BH;
-    bh = blockIdx.x - j * p.BH;
+    j = blockIdx.x / n_heads;
+    bh = blockIdx.x - j * n_heads;
   } else {  // head-major: resident CTAs share one or two heads' dQ accumulators in L2
     bh = blockIdx.x / n;
     j = blockIdx.x - bh * n;
   }
   const int i_lo = CAUSAL ? j : 0;  // query tiles i_lo .. n-1, visited from n-1 down
   int n_it = n - i_lo;
+  // GQA: walk position qi = g * n + i over query head g of the group and
+  // query tile i (from n-1 down to i_lo, head after head); the first query
+  // head of K/V head bh is qh0
+  int qh0 = bh;
+  if (GQA) {
+    const int h_kv = p.h_q / p.kv_group;
+    qh0 = (bh / h_kv) * p.h_q + (bh % h_kv) * p.kv_group;
+    n_it *= p.kv_group;
+  }
+  auto tile_i = [&](int qi) { return GQA ? qi % n : qi; };
+  auto head_q = [&](int qi) { return GQA ? qh0 + qi / n : bh; };
   if (MASK) {  // only the query tiles holding a visible pair with key tile j
     n_it = 0;
     for (int i = 0; i < n; ++i) n_it += mask_tile_visible(p.mask, i, j) ? 1 : 0;
   }
   // every role walks the same query tiles, from the last down
   const int i_first = MASK ? mask_prev_query_tile(p.mask, j, n) : n - 1;
-  auto i_next = [&](int i) { return MASK ? mask_prev_query_tile(p.mask, j, i) : i - 1; };
+  auto i_next = [&](int i) {
+    if (GQA) return (i % n) > i_lo ? i - 1 : (i / n + 1) * n + (n - 1);
+    return MASK ? mask_prev_query_tile(p.mask, j, i) : i - 1;
+  };
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < L::kNumBars; ++b) {
@@ -274,7 +293,9 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         tma_load_3d(sbase + L::kVOff + c * kBSub, &p.tm_v, c * 64, j * kBTile, bh, bar(L::kBarKV));
       }
       int issued_q = 0, issued_do = 0;  // loads issued per ring
-      for (int it = 0, i = i_first; it < n_it; ++it, i = i_next(i)) {
+      for (int it = 0, qi = i_first; it < n_it; ++it, qi = i_next(qi)) {
+        const int i = tile_i(qi);
+        const int qh = head_q(qi);
         const int s = it % L::kQStages;
         const uint32_t ph = ((it / L::kQStages) & 1) ^ 1;
         const int sd = it % L::kDOStages;
@@ -283,9 +304,9 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kTileBytes + L::kVecBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sbase + L::kQOff + s * L::kTileBytes + c * kBSub, &p.tm_q, c * 64, i * kBTile, bh,
+          tma_load_3d(sbase + L::kQOff + s * L::kTileBytes + c * kBSub, &p.tm_q, c * 64, i * kBTile, qh,
                       bar(L::kBarQFull + s));
-        const size_t vrow = (size_t)bh * p.Npad + (size_t)i * kBTile;
+        const size_t vrow = (size_t)qh * p.Npad + (size_t)i * kBTile;
         bulk_load(sbase + L::kVecOff + s * L::kVecBytes, p.row_lse2 + vrow, kBTile * 4, bar(L::kBarQFull + s));
         bulk_load(sbase + L::kVecOff + s * L::kVecBytes + kBTile * 4, p.row_d + vrow, kBTile * 4,
                   bar(L::kBarQFull + s));
@@ -295,7 +316,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
         mbar_arrive_expect_tx(bar(L::kBarDOFull + sd), L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sbase + L::kDOOff + sd * L::kTileBytes + c * kBSub, &p.tm_do, c * 64, i * kBTile, bh,
+          tma_load_3d(sbase + L::kDOOff + sd * L::kTileBytes + c * kBSub, &p.tm_do, c * 64, i * kBTile, qh,
                       bar(L::kBarDOFull + sd));
         ATTN_TRACE_AT(blockIdx.x, it, 14);
         issued_do = it + 1;
@@ -444,7 +465,8 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     const float c_log2 = p.scale_log2;
     const bool key_dead = k_glob >= p.N;
     bool ok = true;
-    for (int it = 0, i = i_first; it < n_it; ++it, i = i_next(i)) {
+    for (int it = 0, qi = i_first; it < n_it; ++it, qi = i_next(qi)) {
+      const int i = tile_i(qi);
       const int s = it % L::kQStages;
       // LSE2 / D vectors arrive with Q_i on the stage's barrier
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + s), (it / L::kQStages) & 1, ctl, kBWhereEw + 3));
@@ -593,7 +615,9 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
     const int tid = threadIdx.x - 384;
     const uint32_t tDQ = tmem + ((uint32_t)(quad * 32) << 16) + L::kColDQ;
     bool ok = true;
-    for (int it = 0, i = i_first; it < n_it; ++it, i = i_next(i)) {
+    for (int it = 0, qi = i_first; it < n_it; ++it, qi = i_next(qi)) {
+      const int i = tile_i(qi);
+      const int qh = head_q(qi);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 9);
@@ -615,8 +639,8 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       // engine as a bulk FP32 reduce-add.  The staging tile is reused once
       // the previous tile's bulk read of it has finished.
       float* stg = reinterpret_cast<float*>(smem + L::kStgOff);
-      float* gdst = p.dq_acc + ((size_t)bh * p.n_tiles + i) * (size_t)(D * kBTile);
-      int* ticket = DETERMINISTIC ? p.tickets + (size_t)bh * p.n_tiles + i : nullptr;
+      float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(D * kBTile);
+      int* ticket = DETERMINISTIC ? p.tickets + (size_t)qh * p.n_tiles + i : nullptr;
       constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
 #pragma unroll
       for (int r = 0; r < L::kStgRounds; ++r) {
@@ -682,7 +706,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
 template <bool CAUSAL, bool DET>
 cudaError_t launch_bwd2_main(const BwdParams& p, cudaStream_t stream);
 
-template <int D, bool CAUSAL, bool DET, bool MASK = false>
+template <int D, bool CAUSAL, bool DET, bool MASK = false, bool GQA = false>
 cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const LaunchEvents* evs) {
   using L = BwdLayout<D>;
   auto mark = [&](int i) {
@@ -701,19 +725,20 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
   mark(1);
   bool paired = false;
   if constexpr (D == 128) {
-    if (p.pair_mode && !MASK) {
+    if (p.pair_mode && !MASK && !GQA) {
       cudaError_t e = launch_bwd2_main<CAUSAL, DET>(p, stream);
       if (e != cudaSuccess) return e;
       paired = true;
     }
   }
   if (!paired) {
-    auto kernel = bwd_kernel<D, CAUSAL, DET, MASK>;
+    auto kernel = bwd_kernel<D, CAUSAL, DET, MASK, GQA>;
     // setmaxnreg.inc waits for registers the dec released: the split must
     // match what the launch hands out
     cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, nullptr);
     if (e != cudaSuccess) return e;
-    kernel<<<p.BH * p.n_tiles, L::kThreads, L::kSmemBytes, stream>>>(p);
+    const int n_heads = GQA ? p.BH / p.kv_group : p.BH;  // one CTA per (K/V head, key tile)
+    kernel<<<n_heads * p.n_tiles, L::kThreads, L::kSmemBytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -88,6 +88,10 @@ struct BwdParams {
   float scale_log2;
   int pair_mode;  // 1: CTA-pair main kernel (d = 128) and its accumulator layout
   MaskSpec mask;  // masked instances only
+  // grouped-query instances: BH counts query heads; h_q query heads per batch
+  // entry, kv_group of them per K/V head
+  int h_q;
+  int kv_group;
 };
 
 // Optional events recorded on the launch stream around each backward kernel:
@@ -117,6 +121,9 @@ cudaError_t launch_fwd_fp8(const FwdParams& p, bool causal, cudaStream_t s);
 // Masked forward / backward (p.mask), d = 64 or 128 (attn_masked.cu).
 cudaError_t launch_fwd_masked(const FwdParams& p, int d, cudaStream_t s);
 cudaError_t launch_bwd_masked(const BwdParams& p, int d, bool deterministic, cudaStream_t s, const LaunchEvents* ev);
+// Grouped-query backward (p.kv_group > 1), d = 64 or 128 (attn_masked.cu).
+cudaError_t launch_bwd_gqa(const BwdParams& p, int d, bool causal, bool deterministic, cudaStream_t s,
+                           const LaunchEvents* ev);
 struct QuantParams {
   const void* q;
   const void* k;

@@ -270,6 +270,18 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* sq
                  void* o, float* lse, int B, int H, int N, int d, int causal, float scale, cudaStream_t stream);
 
 /*
+ * Backward with grouped-query attention: gradients of attn_fwd_gqa.
+ *   q, o, dO, dq [B,H,N,d], lse [B,H,N]; k, v, dk, dv [B,H_kv,N,d];
+ *   H % H_kv == 0.  dk and dv of a K/V head sum the contributions of its
+ *   H / H_kv query heads.  Workspace: attn_bwd_workspace_bytes(B, H, N, ...)
+ *   (per query head).  Other arguments as attn_bwd (the CTA-pair mode does
+ *   not apply).
+ */
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d_qk, int d_v, int causal,
+                 float scale, int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronises ``stream``, then returns and clears the device status word of
  * the current device: ATTN_OK, or the first error a kernel recorded since the
  * last call (ATTN_ERR_TIMEOUT, ATTN_ERR_BOUNDS).  If the stream itself

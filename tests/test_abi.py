@@ -247,3 +247,8 @@ def test_gqa_argument_errors(lib):
     assert f(p, p, p, p, p, 1, 8, 3, 1, 1000, 128, 128, 0.1, 2, p, ws, None) == A.ATTN_ERR_INVALID_ARG
     assert f(p, p, p, p, p, 1, 8, 2, 0, 1000, 128, 128, 0.1, 2, p, ws, None) == A.ATTN_ERR_INVALID_ARG
     assert f(p, p, p, p, p, 1, 8, 2, 1, 1000, 128, 128, 0.1, 2, p, ws - 1, None) == A.ATTN_ERR_WORKSPACE
+    ws2 = A.attn_bwd_workspace_bytes(1, 8, 256, 128, 128, 0)
+    g = L.attn_bwd_gqa
+    assert g(p, p, p, p, p, p, p, p, p, 1, 8, 3, 256, 128, 128, 0, 0.1, 0, p, ws2, None) == A.ATTN_ERR_INVALID_ARG
+    assert g(p, p, p, p, p, p, p, p, p, 1, 8, 16, 256, 128, 128, 0, 0.1, 0, p, ws2, None) == A.ATTN_ERR_INVALID_ARG
+    assert g(p, p, p, p, p, p, p, p, p, 1, 8, 2, 256, 128, 128, 0, 0.1, 0, p, ws2 - 1, None) == A.ATTN_ERR_WORKSPACE

@@ -83,3 +83,65 @@ def test_splitkv_gqa(A, H, H_kv, N_q, N_k, n_splits):
     G.check_status(A)
     o_ref, lse_ref = _oracle(G.f64(q), G.f64(k), G.f64(v), False)
     G.assert_fwd_close(G.f64(o), G.f64(lse), o_ref, lse_ref, f"H{H}/{H_kv} Nq{N_q} Nk{N_k} splits{n_splits}")
+
+
+def _oracle_bwd(q, k, v, do, causal):
+    """dQ per query head; dK, dV of a K/V head summed over its query heads."""
+    B, H = q.shape[:2]
+    H_kv = k.shape[1]
+    g = H // H_kv
+    scale = 1 / math.sqrt(q.shape[-1])
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            a, kb, c = ora.backward_head(q[b, h], k[b, h // g], v[b, h // g], do[b, h], scale, causal)
+            dq[b, h] = a
+            dk[b, h // g] += kb
+            dv[b, h // g] += c
+    return dq, dk, dv
+
+
+def _run_bwd_gqa(A, q, k, v, do, causal, det):
+    torch = G.torch_mod()
+    B, H, N, dqk = q.shape
+    H_kv, dv_ = k.shape[1], v.shape[-1]
+    scale = 1 / math.sqrt(dqk)
+    o = torch.empty((B, H, N, dv_), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    A.attn_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, dqk, dv_, causal, scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nb = A.attn_bwd_workspace_bytes(B, H, N, dqk, dv_, det)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    A.attn_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, B, H, H_kv, N, dqk, dv_, causal, scale, det, ws, nb)
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,H_kv", [(8, 2), (6, 1), (4, 4)])
+@pytest.mark.parametrize("N", [1, 257, 640])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("det", [0, 1])
+def test_backward_gqa(A, d, H, H_kv, N, causal, det):
+    B = 2
+    q, k, v = _inputs(B, H, H_kv, N, N, d, d, seed=33)
+    do = synth.decode_inputs_torch(synth.DecodeShape(B, H, N, 1, d, d), seed=34)["q"]
+    grads = _run_bwd_gqa(A, q, k, v, do, causal, det)
+    G.check_status(A)
+    refs = _oracle_bwd(G.f64(q), G.f64(k), G.f64(v), G.f64(do), bool(causal))
+    for name, got, ref in zip(("dq", "dk", "dv"), grads, refs):
+        G.assert_grad_close(name, G.f64(got), ref)
+
+
+def test_backward_gqa_deterministic_is_bit_identical(A):
+    torch = G.torch_mod()
+    B, H, H_kv, N, d = 2, 8, 2, 1000, 128
+    q, k, v = _inputs(B, H, H_kv, N, N, d, d, seed=35)
+    do = synth.decode_inputs_torch(synth.DecodeShape(B, H, N, 1, d, d), seed=36)["q"]
+    for causal in (0, 1):
+        runs = [_run_bwd_gqa(A, q, k, v, do, causal, 1) for _ in range(3)]
+        G.check_status(A)
+        for r in runs[1:]:
+            for a, b in zip(runs[0], r):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
