@@ -277,9 +277,11 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public API: pinned host buffers in, results out.
     # Every (b, h) is independent, so the step runs as n_chunks groups of
-    # heads on three streams: the inputs of group c+1 go up and the results
-    # of group c-1 come down while group c computes (every byte still crosses
-    # the link inside the timed region, every step).
+    # heads: inputs go up on one stream, results come down on another, and
+    # the groups' kernels run on n_cs compute streams (round-robin, one
+    # workspace each), so copies overlap kernels and neighbouring groups'
+    # small grids share the GPU (every byte still crosses the link inside the
+    # timed region, every step).
     hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
     ho, hlse, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, lse, dq, dk, dv))
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
@@ -294,7 +296,9 @@ def run_ours(args, world, rank, local):
     pairs_out = [(flat(dst), flat(src)) for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv))]
     dev_t = [flat(x) for x in (q, k, v, o, do, lse, dq, dk, dv)]
     cws = A.attn_bwd_workspace_bytes(1, hc, N, d, d, args.det)
-    cwsb = torch.empty(cws, dtype=torch.uint8, device=dev)
+    n_cs = max(1, min(args.e2e_streams, n_chunks))  # compute streams, groups dealt round-robin
+    cwsb = [torch.empty(cws, dtype=torch.uint8, device=dev) for _ in range(n_cs)]
+    s_comp = [stream] + [torch.cuda.Stream(dev) for _ in range(n_cs - 1)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
     ev_in, ev_done, ev_out = [ev() for _ in range(n_chunks)], [ev() for _ in range(n_chunks)], [ev() for _ in range(n_chunks)]
@@ -305,28 +309,33 @@ def run_ours(args, world, rank, local):
         ev_start.record(stream)
         s_in.wait_event(ev_start)
         s_out.wait_event(ev_start)
+        for cs in s_comp[1:]:
+            cs.wait_event(ev_start)
         for c in range(n_chunks):
             sl = slice(c * hc, (c + 1) * hc)
+            cs = s_comp[c % n_cs]
             if not first[0]:
                 s_in.wait_event(ev_done[c])  # the previous step's group c no longer reads these inputs
             with torch.cuda.stream(s_in):
                 for dst, src in pairs_in:
                     dst[sl].copy_(src[sl], non_blocking=True)
             ev_in[c].record(s_in)
-            stream.wait_event(ev_in[c])
+            cs.wait_event(ev_in[c])
             if not first[0]:
-                stream.wait_event(ev_out[c])  # the previous step's results of group c are out
+                cs.wait_event(ev_out[c])  # the previous step's results of group c are out
             cq, ck, cv, co, cdo, clse, cdq, cdk, cdv = (x[sl] for x in dev_t)
-            A.attn_fwd(cq, ck, cv, co, clse, 1, hc, N, d, d, args.causal, scale, stream)
-            A.attn_bwd(cq, ck, cv, co, cdo, clse, cdq, cdk, cdv, 1, hc, N, d, d, args.causal, scale, args.det, cwsb,
-                       cws, stream)
-            ev_done[c].record(stream)
+            A.attn_fwd(cq, ck, cv, co, clse, 1, hc, N, d, d, args.causal, scale, cs)
+            A.attn_bwd(cq, ck, cv, co, cdo, clse, cdq, cdk, cdv, 1, hc, N, d, d, args.causal, scale, args.det,
+                       cwsb[c % n_cs], cws, cs)
+            ev_done[c].record(cs)
             s_out.wait_event(ev_done[c])
             with torch.cuda.stream(s_out):
                 for dst, src in pairs_out:
                     dst[sl].copy_(src[sl], non_blocking=True)
             ev_out[c].record(s_out)
         first[0] = False
+        for cs in s_comp[1:]:
+            stream.wait_stream(cs)
         stream.wait_stream(s_out)
         stream.wait_stream(s_in)
 
@@ -384,7 +393,8 @@ def run_ours(args, world, rank, local):
                              "backward_incl_pre_convert": 2.5 * f_fwd / ((prof["ms_bwd_pre"] + prof["ms_bwd_main"] + prof["ms_bwd_convert"]) / max(prof["launches_bwd_main"], 1) / 1e3) / 1e12 if prof["launches_bwd_main"] else None},
         "clocks": clk, "gpu_launches": launches,
         "e2e": {"value": world * f_step / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "head_groups": n_chunks},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "head_groups": n_chunks,
+                "compute_streams": n_cs},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
@@ -536,6 +546,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="head groups pipelined through host copies and compute in the e2e leg")
+    ap.add_argument("--e2e-streams", type=int, default=2, help="compute streams the e2e leg deals its groups to")
     ap.add_argument("--case", choices=("step", "fp8", "splitkv", "masked"), default="step",
                     help="step: the benchmark contract; others time the library's other paths")
     ap.add_argument("--Nq", type=int, default=1)
