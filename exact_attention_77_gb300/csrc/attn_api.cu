@@ -120,7 +120,45 @@ int encoder(EncodeTiledFn* out) {
 // 3-D view [BH, N, d] of a contiguous tensor of bf16 (elem_bytes 2) or of
 // 8-bit codes (elem_bytes 1); box 128 bytes of d x box_rows rows x 1 with the
 // 128-byte swizzle; rows past N read as zero.
+// Encoded descriptors are kept in a small cache keyed by every input of the
+// encoding (a descriptor holds only the address and the shape, so a reused
+// address with the same shape gets an identical descriptor).
+struct MapKey {
+  const void* ptr;
+  int BH, N, d, box_rows, elem_bytes;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && BH == o.BH && N == o.N && d == o.d && box_rows == o.box_rows && elem_bytes == o.elem_bytes;
+  }
+};
+constexpr int kMapCache = 64;
+struct MapCache {
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  int used = 0, next = 0;
+};
+MapCache g_maps;
+
+int make_map_uncached(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows, int elem_bytes);
+
 int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128, int elem_bytes = 2) {
+  const MapKey k{ptr, BH, N, d, box_rows, elem_bytes};
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < g_maps.used; ++i)
+      if (g_maps.key[i] == k) {
+        *map = g_maps.map[i];
+        return ATTN_OK;
+      }
+  }
+  if (int st = make_map_uncached(map, ptr, BH, N, d, box_rows, elem_bytes)) return st;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int slot = g_maps.used < kMapCache ? g_maps.used++ : (g_maps.next++ % kMapCache);
+  g_maps.key[slot] = k;
+  g_maps.map[slot] = *map;
+  return ATTN_OK;
+}
+
+int make_map_uncached(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows, int elem_bytes) {
   EncodeTiledFn enc;
   if (int st = encoder(&enc)) return st;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
