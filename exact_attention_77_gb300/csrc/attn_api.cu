@@ -28,6 +28,7 @@ struct Settings {
   int fwd_max_ctas = 0;  // persistent forward grid size (0: one CTA per free SM slot)
   int fwd_persist = -1;  // -1: by sequence length; 0 / 1 forces
   int bwd_pair = 0;      // 1: d = 128 backward on CTA pairs
+  int bwd_persist = -1;  // -1: by sequence length; 0 / 1 forces persistent backward CTAs
   int merge_pdl = 1;     // 1: split-KV merge as a programmatic dependent launch
   float fp8_tau = 4.f;   // FP8 forward: rescale threshold (P stored as e4m3(2^(8 - tau) P))
   float tau = 8.0f;
@@ -79,6 +80,7 @@ Settings settings() {
     if (const char* e = getenv("ATTN_FWD_MAX_CTAS")) g_settings.fwd_max_ctas = atoi(e);
     if (const char* e = getenv("ATTN_FWD_PERSIST")) g_settings.fwd_persist = atoi(e);
     if (const char* e = getenv("ATTN_BWD_PAIR")) g_settings.bwd_pair = atoi(e) != 0;
+    if (const char* e = getenv("ATTN_BWD_PERSIST")) g_settings.bwd_persist = atoi(e);
     if (const char* e = getenv("ATTN_MERGE_PDL")) g_settings.merge_pdl = atoi(e) != 0;
     if (const char* e = getenv("ATTN_FP8_TAU")) {
       const int v = atoi(e);
@@ -614,6 +616,10 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)
   p.pair_mode = (d_qk == 128 && cfg.bwd_pair && mask == nullptr && !gqa) ? 1 : 0;
   if (mask != nullptr) p.mask = *mask;
+  // persistent CTAs when the (head, key tile) units are short (measured on
+  // GB300: +5-15 % at N <= 2048; at N = 4096 +1-5 % with atomic dQ and
+  // mixed with tickets; slower at N = 16384)
+  p.persist = cfg.bwd_persist >= 0 ? cfg.bwd_persist : ((N <= 2048 || (N <= 4096 && !deterministic)) ? 1 : 0);
   if (p.pair_mode) {
     if (int st = make_map(&p.tm_q_half, q, BH, N, d_qk, 64)) return st;
     if (int st = make_map(&p.tm_do_half, dO, BH, N, d_v, 64)) return st;

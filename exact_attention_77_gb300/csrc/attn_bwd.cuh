@@ -706,6 +706,10 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
 template <bool CAUSAL, bool DET>
 cudaError_t launch_bwd2_main(const BwdParams& p, cudaStream_t stream);
 
+// Persistent main kernel for short sequences (attn_bwd_persist.cuh).
+template <int D, bool CAUSAL, bool DET>
+cudaError_t launch_bwd_persist_main(const BwdParams& p, cudaStream_t stream);
+
 template <int D, bool CAUSAL, bool DET, bool MASK = false, bool GQA = false>
 cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const LaunchEvents* evs) {
   using L = BwdLayout<D>;
@@ -729,6 +733,13 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
       cudaError_t e = launch_bwd2_main<CAUSAL, DET>(p, stream);
       if (e != cudaSuccess) return e;
       paired = true;
+    }
+  }
+  if constexpr (!MASK && !GQA) {
+    if (!paired && p.persist) {
+      cudaError_t e = launch_bwd_persist_main<D, CAUSAL, DET>(p, stream);
+      if (e != cudaSuccess) return e;
+      paired = true;  // (the main kernel has run: skip the one-unit launch)
     }
   }
   if (!paired) {

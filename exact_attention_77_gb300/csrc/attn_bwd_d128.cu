@@ -1,5 +1,6 @@
 // Backward kernel instances for d_qk = d_v = 128.
 #include "attn_bwd2.cuh"
+#include "attn_bwd_persist.cuh"
 
 namespace attn {
 

@@ -1,5 +1,6 @@
 // Backward kernel instances for d_qk = d_v = 64.
 #include "attn_bwd.cuh"
+#include "attn_bwd_persist.cuh"
 
 namespace attn {
 

@@ -92,6 +92,7 @@ struct BwdParams {
   // entry, kv_group of them per K/V head
   int h_q;
   int kv_group;
+  int persist;  // 1: persistent CTAs (one per SM) over the (head, key tile) units
 };
 
 // Optional events recorded on the launch stream around each backward kernel:
