@@ -345,6 +345,18 @@ int attn_set_rescale_threshold(float tau);
 int attn_set_bwd_pair(int enable);
 
 /*
+ * Backward main kernel selection for later attn_bwd / attn_bwd_noalloc calls:
+ * mode = 1 runs the persistent kernel (one CTA per SM taking the (head, key
+ * tile) units in rounds), 0 the kernel with one CTA per unit, -1 (the
+ * default; also ATTN_BWD_PERSIST at first use) chooses by size: persistent for
+ * N <= 2048, and for N <= 4096 in atomic mode.  Results meet the same
+ * tolerances either way; deterministic mode is bit-identical run to run with
+ * either kernel (the two may differ from each other in the last bits).
+ * Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
+ */
+int attn_set_bwd_persist(int mode);
+
+/*
  * Per-kernel timing for benchmarks.  Between attn_profile_start and
  * attn_profile_stop, every attn_fwd / attn_bwd call on any stream also records
  * CUDA events immediately before and after each of its kernel launches, on

@@ -266,3 +266,50 @@ def test_backward_pair_deterministic_is_bit_identical(A, pair_mode):
         for r in runs[1:]:
             for a, b in zip(runs[0], r):
                 assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.fixture(params=[0, 1], ids=["one_unit_per_cta", "persistent"])
+def bwd_kernel_mode(A, request):
+    A.attn_set_bwd_persist(request.param)
+    yield request.param
+    A.attn_set_bwd_persist(-1)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 100, 257, 1000])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("det", [0, 1])
+def test_backward_both_kernels(A, bwd_kernel_mode, d, N, causal, det):
+    """The one-unit and the persistent backward kernels, each forced, on small
+    and ragged sizes with several heads (persistent CTAs take several units)."""
+    B, H = 2, 3
+    t = G.inputs(B, H, N, d, d, seed=41)
+    o, lse = G.run_fwd(A, t, causal)
+    dq, dk, dv = G.run_bwd(A, t, o, lse, causal, det)
+    G.check_status(A)
+    q, k, v, do = (G.f64(t[n]) for n in ("q", "k", "v", "do"))
+    refs = ora.backward(q, k, v, do, 1.0 / math.sqrt(d), bool(causal))
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        G.assert_grad_close(name, G.f64(got), ref)
+
+
+def test_persistent_backward_many_units_per_cta(A):
+    """More units than SMs (several rounds per CTA), both dQ modes, causal and
+    not; deterministic results bit-identical over repeats."""
+    torch = G.torch_mod()
+    A.attn_set_bwd_persist(1)
+    try:
+        B, H, N, d = 4, 16, 1024, 128  # 512 units
+        t = G.inputs(B, H, N, d, d, seed=42)
+        for causal in (0, 1):
+            o, lse = G.run_fwd(A, t, causal)
+            runs = [G.run_bwd(A, t, o, lse, causal, 1) for _ in range(2)]
+            G.check_status(A)
+            for a, b in zip(runs[0], runs[1]):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+            q, k, v, do = (G.f64(t[n][:1, :2]) for n in ("q", "k", "v", "do"))
+            refs = ora.backward(q, k, v, do, 1.0 / math.sqrt(d), bool(causal))
+            for name, got, ref in zip(("dq", "dk", "dv"), runs[0], refs):
+                G.assert_grad_close(name, G.f64(got[:1, :2]), ref)
+    finally:
+        A.attn_set_bwd_persist(-1)
