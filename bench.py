@@ -546,7 +546,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="head groups pipelined through host copies and compute in the e2e leg")
-    ap.add_argument("--e2e-streams", type=int, default=2, help="compute streams the e2e leg deals its groups to")
+    ap.add_argument("--e2e-streams", type=int, default=3, help="compute streams the e2e leg deals its groups to")
     ap.add_argument("--case", choices=("step", "fp8", "splitkv", "masked"), default="step",
                     help="step: the benchmark contract; others time the library's other paths")
     ap.add_argument("--Nq", type=int, default=1)
