@@ -190,7 +190,11 @@ bool fwd_dims_ok(int d_qk, int d_v) {
   return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 192 && d_v == 128);
 }
 
-bool bwd_dims_ok(int d_qk, int d_v) { return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128); }
+bool bwd_dims_ok(int d_qk, int d_v) {
+  return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 192 && d_v == 128);
+}
+// masked forward and backward: one head dim for Q, K and V
+bool masked_dims_ok(int d_qk, int d_v) { return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128); }
 
 struct WorkspaceLayout {
   size_t lse2, d, acc, tickets, total;
@@ -603,7 +607,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if (H_kv < 1 || H_kv > H || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (int st = check_common(B, H, N, scale, causal)) return st;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
-  if (!bwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
+  if (!bwd_dims_ok(d_qk, d_v) || (mask != nullptr && !masked_dims_ok(d_qk, d_v))) return ATTN_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return ATTN_ERR_MISALIGNED;
@@ -659,6 +663,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   cudaError_t e;
   if (mask != nullptr)
     e = attn::launch_bwd_masked(p, d_qk, deterministic != 0, stream, prof ? &evs : nullptr);
+  else if (d_qk == 192)
+    e = attn::launch_bwd_d192(p, causal != 0, deterministic != 0, gqa, stream, prof ? &evs : nullptr);
   else if (gqa)
     e = attn::launch_bwd_gqa(p, d_qk, causal != 0, deterministic != 0, stream, prof ? &evs : nullptr);
   else
@@ -718,7 +724,7 @@ int attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float*
   attn::FwdParams p;
   memset(&p, 0, sizeof(p));
   if (int st = make_mask(&p.mask, N, window_left, window_right, block_mask)) return st;
-  if (!bwd_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
+  if (!masked_dims_ok(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
   if (block_mask != nullptr && !aligned16(block_mask)) return ATTN_ERR_MISALIGNED;
   const Settings cfg = settings();

@@ -1,0 +1,587 @@
+// Backward attention for d_qk = 192, d_v = 128 (sm_103a).
+//
+// The same graph of five products and two elementwise steps as bwd_kernel
+// ("FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
+// Asymmetric Hardware Scaling", Figure 2 and Table 3), for the head shape of
+// the forward's third configuration (d_qk = 192, d_v = 128):
+//     S^T  = K_j Q_i^T   (K = 192)        dP^T = V_j dO_i^T   (K = 128)
+//     dV  += P^T dO_i    (N = 128)        dK  += dS^T Q_i     (N = 192)
+//     dQ_i = dS K_j      (N = 192)
+//
+// What differs from bwd_kernel is the tensor-memory plan.  Its layout would
+// need dV (128) + dK (192) + S^T (128) + dP^T (128) = 576 columns, over the
+// 512 an SM has.  Here S^T and dP^T take turns in one 128-column region X:
+// the compute warpgroups read S^T into registers (they keep P there for dS
+// anyway) and pack bf16 P^T into a separate 64-column region PK; once both
+// warpgroups have done so, dP^T is written over X.  dS^T is packed into PK
+// after the dV product has read P^T.  dQ_i (192 columns) spans X and PK, so
+// the next tile's S^T waits for the dQ read-out.  Totals: dV 128 + dK 192 +
+// X 128 + PK 64 = 512.
+//
+// Shared memory: K_j 48 KiB, V_j 32 KiB, one Q_i stage 48 KiB, one dO_i stage
+// 32 KiB, dS 32 KiB, the dQ staging tile 32 KiB: 225 KiB.
+//
+// Warp roles as in bwd_kernel: warp 0 producer, warp 1 MMA issuer, warps
+// 4-11 two compute warpgroups (queries 64h .. 64h+63 each), warps 12-15 the
+// dQ warpgroup.  Atomic or deterministic dQ accumulation, causal or not,
+// grouped-query heads.
+#pragma once
+
+#include <type_traits>
+
+#include "attn_bwd.cuh"
+
+namespace attn {
+
+struct Bwd192Layout {
+  static constexpr int kDQK = 192;
+  static constexpr int kDV = 128;
+  static constexpr int kQKBytes = kBTile * kDQK * 2;  // K_j, Q_i: three 64-column chunks
+  static constexpr int kVBytes = kBTile * kDV * 2;    // V_j, dO_i: two chunks
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kQKBytes;
+  static constexpr int kQOff = kVOff + kVBytes;
+  static constexpr int kDOOff = kQOff + kQKBytes;
+  static constexpr int kDSOff = kDOOff + kVBytes;  // dS (bf16 128x128), MN-major for the dQ product
+  static constexpr int kDSBytes = kBTile * kBTile * 2;
+  static constexpr int kStgOff = kDSOff + kDSBytes;  // dQ_i staging: 64 columns per round
+  static constexpr int kStgBytes = 32 * 1024;
+  static constexpr int kStgRounds = kBTile * kDQK * 4 / kStgBytes;  // 3
+  static constexpr int kVecOff = kStgOff + kStgBytes;  // -LSE2[128], -D[128] fp32 of Q_i
+  static constexpr int kVecBytes = 2 * kBTile * 4;
+  static constexpr int kBarOff = kVecOff + kVecBytes;
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarQFull = 1;
+  static constexpr int kBarQEmpty = 2;
+  static constexpr int kBarDOFull = 3;
+  static constexpr int kBarDOEmpty = 4;
+  static constexpr int kBarSFull = 5;
+  static constexpr int kBarDPFull = 6;
+  static constexpr int kBarPReady = 7;  // + half m (256 arrivals each)
+  static constexpr int kBarDSFull = 9;  // + half m
+  static constexpr int kBarDQFull = 11;
+  static constexpr int kBarDQFree = 12;  // 128 arrivals: every dQ column read
+  static constexpr int kBarAccDone = 13;
+  static constexpr int kNumBars = 14;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kQOff % 1024 == 0 && kDOOff % 1024 == 0 &&
+                    kDSOff % 1024 == 0 && kStgOff % 1024 == 0,
+                "128-byte-swizzled tiles start on 1024-byte boundaries");
+  // tensor memory columns
+  static constexpr int kColDV = 0;
+  static constexpr int kColDK = kColDV + kDV;
+  static constexpr int kColX = kColDK + kDQK;  // S^T, then dP^T (fp32, 128 columns)
+  static constexpr int kColPK = kColX + 128;   // P^T, then dS^T (bf16 packed, 64 columns)
+  static constexpr int kColDQ = kColX;         // dQ_i fp32 over X and PK (192 columns)
+  static_assert(kColPK + 64 == 512 && kColDQ + kDQK == 512, "tensor-memory plan");
+  static constexpr int kThreads = 512;
+  static constexpr int kLaunchRegs = 128;
+  static constexpr int kCtlRegs = 112;
+  static constexpr int kComputeRegs = 128;
+  static constexpr int kDqRegs = 144;
+  static_assert(kCtlRegs * 128 + kComputeRegs * 256 + kDqRegs * 128 <= kLaunchRegs * kThreads, "register split");
+};
+
+enum : int { kB192WhereProd = 160, kB192WhereMma = 170, kB192WhereEw = 180, kB192WhereDq = 190 };
+
+// Preprocess for this head shape: -D and -LSE2 as bwd_pre_kernel<128> (dO and
+// O rows are d_v = 128 wide), zeroing the 192-wide dQ accumulator.
+__global__ void __launch_bounds__(256) bwd192_pre_kernel(BwdParams p) {
+  constexpr int kLanes = 16;  // 128 / 8
+  constexpr int kRowsPerBlock = 256 / kLanes;
+  const int sub = threadIdx.x % kLanes;
+  const long row = (long)blockIdx.x * kRowsPerBlock + threadIdx.x / kLanes;
+  const long total_rows = (long)p.BH * p.Npad;
+  const bool in_range = row < total_rows;
+  const int bh = in_range ? (int)(row / p.Npad) : 0;
+  const int i = in_range ? (int)(row - (long)bh * p.Npad) : p.N;
+  float acc = 0.f;
+  if (i < p.N) {
+    const size_t off = ((size_t)bh * p.N + i) * 128 + sub * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dO) + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 fa = __bfloat1622float2(a2[k]);
+      const float2 fb = __bfloat1622float2(b2[k]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, kLanes);
+  if (in_range && sub == 0) {
+    p.row_d[row] = -acc;
+    p.row_lse2[row] = i < p.N ? -p.lse[(size_t)bh * p.N + i] * 1.4426950408889634f : -INFINITY;
+  }
+  const size_t n4 = (size_t)p.BH * p.Npad * Bwd192Layout::kDQK / 4;
+  float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
+  for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += (size_t)gridDim.x * blockDim.x)
+    acc4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (p.tickets != nullptr)
+    for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < (size_t)p.BH * p.n_tiles;
+         k += (size_t)gridDim.x * blockDim.x)
+      p.tickets[k] = 0;
+}
+
+// dQ = scale * accumulator as bf16 [BH, N, 192]; accumulator per (bh, tile)
+// in [48 column groups][128 rows][4] order.  One warp per row: lane g takes
+// groups g and, for g < 16, g + 32.
+__global__ void __launch_bounds__(256) dq192_convert_kernel(BwdParams p) {
+  constexpr int kGroups = Bwd192Layout::kDQK / 4;
+  const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= (long)p.BH * p.N) return;
+  const int bh = (int)(row / p.N);
+  const int i = (int)(row - (long)bh * p.N);
+  const size_t tile_base = ((size_t)bh * p.n_tiles + (i >> 7)) * kGroups;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.dq) + (size_t)row * Bwd192Layout::kDQK;
+  for (int g = lane; g < kGroups; g += 32) {
+    const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + ((tile_base + g) * 128 + (i & 127)) * 4);
+    uint2 o;
+    o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
+    o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
+    *reinterpret_cast<uint2*>(out + 4 * g) = o;
+  }
+}
+
+template <bool CAUSAL, bool DETERMINISTIC, bool GQA>
+__global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ BwdParams p) {
+  using L = Bwd192Layout;
+  constexpr int DQK = L::kDQK;
+  constexpr int DV = L::kDV;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) report_error(p.status, ATTN_ERR_BOUNDS, 3);
+    return;
+  }
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  // work unit: key tile j of K/V head bh (unit order as in bwd_kernel)
+  const int n = p.n_tiles;
+  const int n_heads = GQA ? p.BH / p.kv_group : p.BH;
+  int j, bh;
+  if (DETERMINISTIC) {
+    j = blockIdx.x / n_heads;
+    bh = blockIdx.x - j * n_heads;
+  } else {
+    bh = blockIdx.x / n;
+    j = blockIdx.x - bh * n;
+  }
+  const int i_lo = CAUSAL ? j : 0;
+  int n_it = n - i_lo;
+  int qh0 = bh;
+  if (GQA) {
+    const int h_kv = p.h_q / p.kv_group;
+    qh0 = (bh / h_kv) * p.h_q + (bh % h_kv) * p.kv_group;
+    n_it *= p.kv_group;
+  }
+  // walk position qi = g * n + i: query head g of the group, query tile i
+  // from n-1 down to i_lo
+  auto tile_i = [&](int qi) { return GQA ? qi % n : qi; };
+  auto head_q = [&](int qi) { return GQA ? qh0 + qi / n : bh; };
+  auto i_next = [&](int qi) {
+    if (GQA) return (qi % n) > i_lo ? qi - 1 : (qi / n + 1) * n + (n - 1);
+    return qi - 1;
+  };
+  const int i_first = n - 1;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < L::kNumBars; ++b) {
+      uint32_t cnt = 1;
+      if (b == L::kBarPReady || b == L::kBarPReady + 1 || b == L::kBarDSFull || b == L::kBarDSFull + 1) cnt = 256;
+      if (b == L::kBarDQFree) cnt = 128;
+      mbar_init(bar(b), cnt);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(L::kCtlRegs));
+    if (warp == 0) {
+      // ============================ producer ============================
+      if (lane == 0) {
+        prefetch_tensormap(&p.tm_q);
+        prefetch_tensormap(&p.tm_k);
+        prefetch_tensormap(&p.tm_v);
+        prefetch_tensormap(&p.tm_do);
+        mbar_arrive_expect_tx(bar(L::kBarKV), L::kQKBytes + L::kVBytes);
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          tma_load_3d(sbase + L::kKOff + c * kBSub, &p.tm_k, c * 64, j * kBTile, bh, bar(L::kBarKV));
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_3d(sbase + L::kVOff + c * kBSub, &p.tm_v, c * 64, j * kBTile, bh, bar(L::kBarKV));
+        int issued_q = 0, issued_do = 0;
+        for (int it = 0, qi = i_first; it < n_it; ++it, qi = i_next(qi)) {
+          const int i = tile_i(qi);
+          const int qh = head_q(qi);
+          const uint32_t ph = (it & 1) ^ 1;
+          if (!mbar_wait(bar(L::kBarQEmpty), ph, ctl, kB192WhereProd)) break;
+          mbar_arrive_expect_tx(bar(L::kBarQFull), L::kQKBytes + L::kVecBytes);
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c)
+            tma_load_3d(sbase + L::kQOff + c * kBSub, &p.tm_q, c * 64, i * kBTile, qh, bar(L::kBarQFull));
+          const size_t vrow = (size_t)qh * p.Npad + (size_t)i * kBTile;
+          bulk_load(sbase + L::kVecOff, p.row_lse2 + vrow, kBTile * 4, bar(L::kBarQFull));
+          bulk_load(sbase + L::kVecOff + kBTile * 4, p.row_d + vrow, kBTile * 4, bar(L::kBarQFull));
+          issued_q = it + 1;
+          if (!mbar_wait(bar(L::kBarDOEmpty), ph, ctl, kB192WhereProd + 1)) break;
+          mbar_arrive_expect_tx(bar(L::kBarDOFull), L::kVBytes);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_3d(sbase + L::kDOOff + c * kBSub, &p.tm_do, c * 64, i * kBTile, qh, bar(L::kBarDOFull));
+          issued_do = it + 1;
+        }
+        // loads in flight land before the CTA exits (one stage per ring)
+        mbar_wait_drain(bar(L::kBarKV), 0, p.timeout_ns);
+        if (issued_q > 0) mbar_wait_drain(bar(L::kBarQFull), (issued_q - 1) & 1, p.timeout_ns);
+        if (issued_do > 0) mbar_wait_drain(bar(L::kBarDOFull), (issued_do - 1) & 1, p.timeout_ns);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ============================ MMA issuer ===========================
+      if (lane == 0) {
+        constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
+        constexpr uint32_t kIdDV = idesc_bf16_f32(128, DV, false, true);    // dV (A in tensor memory)
+        constexpr uint32_t kIdDK = idesc_bf16_f32(128, DQK, false, true);   // dK (A in tensor memory)
+        constexpr uint32_t kIdDQ = idesc_bf16_f32(128, DQK, true, true);    // dQ (A = dS, MN-major)
+        // C = A B^T, A and B [128 x KD] K-major in 64-column chunks kBSub apart
+        auto mma_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base, auto kd) {
+          const uint64_t da = sdesc_sw128(a_base, 16, 1024);
+          const uint64_t db = sdesc_sw128(b_base, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < decltype(kd)::value / 16; ++kk) {
+            const uint32_t off = (kk / 4) * kBSub + (kk % 4) * 32;
+            mma_ss(tmem + d_col, sdesc_advance(da, off), sdesc_advance(db, off), kIdS, kk > 0);
+          }
+        };
+        // C (+)= A[tensor memory: 128 keys x 128 queries, bf16] B, B [128
+        // queries (K) x N] MN-major in 64-column chunks kBSub apart.  A's
+        // queries 64h+32m .. 64h+32m+31 sit in columns kColPK + 32h + 16m
+        // .. +15; half m takes those K steps of both warpgroups h.
+        auto mma_pk_half = [&](uint32_t d_col, uint32_t b_base, uint32_t id, bool acc, int m) {
+          const uint64_t db = sdesc_sw128(b_base, kBSub, 1024);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int kk = 4 * hh + 2 * m + u;
+              mma_ts(tmem + d_col, tmem + L::kColPK + (kk / 4) * 32 + (kk % 4) * 8, sdesc_advance(db, kk * 2048), id,
+                     (acc || m > 0 || hh > 0 || u > 0) ? 1u : 0u);
+            }
+        };
+        bool ok = mbar_wait(bar(L::kBarKV), 0, ctl, kB192WhereMma);
+        tc_fence_after();
+        for (int it = 0; ok && it < n_it; ++it) {
+          const uint32_t ph = it & 1;
+          const uint32_t qs = sbase + L::kQOff;
+          const uint32_t dos = sbase + L::kDOOff;
+          if (!(ok = mbar_wait(bar(L::kBarQFull), ph, ctl, kB192WhereMma + 1))) break;
+          // X and PK hold dQ of the previous tile until it has been read
+          if (it > 0 && !(ok = mbar_wait(bar(L::kBarDQFree), ph ^ 1, ctl, kB192WhereMma + 2))) break;
+          tc_fence_after();
+          mma_kmajor(L::kColX, sbase + L::kKOff, qs, std::integral_constant<int, DQK>{});
+          tc_commit(bar(L::kBarSFull));
+          if (!(ok = mbar_wait(bar(L::kBarDOFull), ph, ctl, kB192WhereMma + 3))) break;
+          // dV on each half of P^T as it lands
+#pragma unroll
+          for (int m = 0; m < 2 && ok; ++m) {
+            if (!(ok = mbar_wait(bar(L::kBarPReady + m), ph, ctl, kB192WhereMma + 4))) break;
+            tc_fence_after();
+            mma_pk_half(L::kColDV, dos, kIdDV, it > 0, m);
+          }
+          if (!ok) break;
+          // both warpgroups have read all of S^T: dP^T goes over it
+          mma_kmajor(L::kColX, sbase + L::kVOff, dos, std::integral_constant<int, DV>{});
+          tc_commit(bar(L::kBarDPFull));
+          tc_commit(bar(L::kBarDOEmpty));  // dO_i's last reader
+#pragma unroll
+          for (int m = 0; m < 2 && ok; ++m) {
+            if (!(ok = mbar_wait(bar(L::kBarDSFull + m), ph, ctl, kB192WhereMma + 6))) break;
+            tc_fence_after();
+            mma_pk_half(L::kColDK, qs, kIdDK, it > 0, m);
+          }
+          if (!ok) break;
+          tc_commit(bar(L::kBarQEmpty));
+          {
+            const uint64_t da = sdesc_sw128(sbase + L::kDSOff, kBSub, 1024);
+            const uint64_t db = sdesc_sw128(sbase + L::kKOff, kBSub, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kBTile / 16; ++kk)
+              mma_ss(tmem + L::kColDQ, sdesc_advance(da, kk * 2048), sdesc_advance(db, kk * 2048), kIdDQ, kk > 0);
+          }
+          tc_commit(bar(L::kBarDQFull));
+        }
+        tc_commit(bar(L::kBarAccDone));
+        mbar_wait_drain(bar(L::kBarAccDone), 0, p.timeout_ns);
+      }
+      __syncwarp();
+    }
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kComputeRegs));
+    // ================= two compute warpgroups (h = 0, 1) =================
+    const int h = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int lrow = quad * 32 + lane;  // tensor-memory lane: key row
+    const int k_glob = j * kBTile + lrow;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tX = tmem + lane_base + L::kColX;
+    const uint32_t tPK = tmem + lane_base + L::kColPK + 32 * h;
+    const float c_log2 = p.scale_log2;
+    const bool key_dead = k_glob >= p.N;
+    const float* vec = reinterpret_cast<const float*>(smem + L::kVecOff);
+    bool ok = true;
+    for (int it = 0, qi = i_first; it < n_it; ++it, qi = i_next(qi)) {
+      const int i = tile_i(qi);
+      const uint32_t ph = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull), ph, ctl, kB192WhereEw + 3));
+      if (!ok) break;
+      const bool diag = CAUSAL && i == j;
+      const bool mask_tile = diag || (j * kBTile + kBTile > p.N);
+      // Phase 1 (S^T in X): P = 2^(S^T * scale * log2e - LSE2) for this
+      // warpgroup's 64 queries, kept in registers and packed as bf16 P^T
+      // into PK columns 32h .. 32h+31.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, ctl, kB192WhereEw));
+      if (!ok) break;
+      tc_fence_after();
+      float pv[64];
+      auto p_chunk = [&](int m, auto masked) {
+        const int c0 = 64 * h + 32 * m;
+        float sv[32];
+        tmem_ld32(tX + c0, sv);
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float4 nl = *reinterpret_cast<const float4*>(vec + c0 + q);  // -LSE2
+          const float2 x01 = __ffma2_rn(make_float2(sv[q], sv[q + 1]), make_float2(c_log2, c_log2), make_float2(nl.x, nl.y));
+          const float2 x23 = __ffma2_rn(make_float2(sv[q + 2], sv[q + 3]), make_float2(c_log2, c_log2), make_float2(nl.z, nl.w));
+          float p0 = ex2_mufu(x01.x), p1 = ex2_mufu(x01.y), p2 = ex2_mufu(x23.x), p3 = ex2_mufu(x23.y);
+          if constexpr (decltype(masked)::value) {
+            const int q0 = i * kBTile + c0 + q;
+            if (key_dead || (diag && q0 < k_glob)) p0 = 0.f;
+            if (key_dead || (diag && q0 + 1 < k_glob)) p1 = 0.f;
+            if (key_dead || (diag && q0 + 2 < k_glob)) p2 = 0.f;
+            if (key_dead || (diag && q0 + 3 < k_glob)) p3 = 0.f;
+          }
+          pv[32 * m + q] = p0;
+          pv[32 * m + q + 1] = p1;
+          pv[32 * m + q + 2] = p2;
+          pv[32 * m + q + 3] = p3;
+          pk[q >> 1] = pack_bf16(p0, p1);
+          pk[(q >> 1) + 1] = pack_bf16(p2, p3);
+        }
+        tmem_st16(tPK + 16 * m, pk);
+      };
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        if (mask_tile) p_chunk(m, std::true_type{});
+        else p_chunk(m, std::false_type{});
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarPReady + m));
+      }
+
+      // Phase 2 (dP^T in X, written after both halves of P^T were ready):
+      // dS = P o (dP - D), packed as dS^T into PK (the dV product has read
+      // P^T: it was issued before dP^T) and written to shared memory as dS.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), ph, ctl, kB192WhereEw + 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint8_t* ds_row = smem + L::kDSOff + h * kBSub + (lrow >> 3) * 1024 + (lrow & 7) * 128;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int c0 = 64 * h + 32 * m;
+        float dp[32];
+        tmem_ld32(tX + c0, dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float4 nd = *reinterpret_cast<const float4*>(vec + kBTile + c0 + q);  // -D
+          const float2 ds01 = __fmul2_rn(make_float2(pv[32 * m + q], pv[32 * m + q + 1]),
+                                         __fadd2_rn(make_float2(dp[q], dp[q + 1]), make_float2(nd.x, nd.y)));
+          const float2 ds23 = __fmul2_rn(make_float2(pv[32 * m + q + 2], pv[32 * m + q + 3]),
+                                         __fadd2_rn(make_float2(dp[q + 2], dp[q + 3]), make_float2(nd.z, nd.w)));
+          dk[q >> 1] = pack_bf16(ds01.x, ds01.y);
+          dk[(q >> 1) + 1] = pack_bf16(ds23.x, ds23.y);
+        }
+        tmem_st16(tPK + 16 * m, dk);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (4 * m + u) ^ (lrow & 7);
+          *reinterpret_cast<uint4*>(ds_row + unit * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDSFull + m));
+      }
+    }
+    // epilogue: warpgroup h writes dV columns [64h, 64h+64) and dK columns
+    // [96h, 96h+96) of its key row
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, ctl, kB192WhereEw + 4));
+    if (ok) {
+      tc_fence_after();
+      const bool live = !key_dead;
+      const size_t row = (size_t)bh * p.N + (live ? k_glob : 0);
+      uint4* dvrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dv) + row * DV);
+      uint4* dkrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dk) + row * DQK);
+      auto write32 = [&](uint32_t col, uint4* dst, float mul) {
+        float a[32];
+        if (n_it > 0) {
+          tmem_ld32(tmem + lane_base + col, a);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) a[q] = 0.f;
+        }
+        uint32_t pa[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) pa[q] = pack_bf16(a[2 * q] * mul, a[2 * q + 1] * mul);
+        if (live) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
+        }
+      };
+#pragma unroll
+      for (int c0 = 64 * h; c0 < 64 * h + 64; c0 += 32) write32(L::kColDV + c0, dvrow + c0 / 8, 1.f);
+#pragma unroll
+      for (int c0 = 96 * h; c0 < 96 * h + 96; c0 += 32) write32(L::kColDK + c0, dkrow + c0 / 8, p.scale);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kDqRegs));
+    // ========================== dQ warpgroup ===========================
+    // Round r stages dQ columns 64r .. 64r+63 in the accumulator's [48
+    // groups][128 rows][4] order and has the copy engine add them.  Columns
+    // 64 .. 191 are read before round 1 so the tensor-memory columns are
+    // freed after the first round.
+    const int quad = warp & 3;
+    const int qrow = quad * 32 + lane;
+    const int tid = threadIdx.x - 384;
+    const uint32_t tDQ = tmem + ((uint32_t)(quad * 32) << 16) + L::kColDQ;
+    float* stg = reinterpret_cast<float*>(smem + L::kStgOff);
+    bool ok = true;
+    for (int it = 0, qi = i_first; it < n_it; ++it, qi = i_next(qi)) {
+      const int i = tile_i(qi);
+      const int qh = head_q(qi);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kB192WhereDq));
+      if (!ok) break;
+      tc_fence_after();
+      float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(DQK * kBTile);
+      int* ticket = DETERMINISTIC ? p.tickets + (size_t)qh * p.n_tiles + i : nullptr;
+      // stage 16 column groups (64 columns) from v and hand them to the copy engine
+      auto round = [&](int r, const float* v) {
+        if (it > 0 || r > 0) {  // the previous round's bulk read of the staging tile
+          if (tid == 0) bulk_wait_read<0>();
+          __syncwarp();
+          named_bar_sync(1, 128);
+        }
+#pragma unroll
+        for (int g = 0; g < 16; ++g)
+          *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+              make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (tid == 0) {
+          if (DETERMINISTIC && r == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(ticket) != j) {  // key tiles add in ascending order
+              if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
+                if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
+                *ctl.abort = 1;
+                break;
+              }
+            }
+            fence_proxy_async_global();
+          }
+          if (!*ctl.abort) {
+            bulk_reduce_add_f32(gdst + (size_t)r * 16 * kBTile * 4, smem_u32(stg), L::kStgBytes);
+            bulk_commit();
+          }
+        }
+        __syncwarp();
+      };
+      {
+        float a[64];
+        tmem_ld64(tDQ, a);
+        round(0, a);
+      }
+      float b[128];
+      tmem_ld64(tDQ + 64, *reinterpret_cast<float(*)[64]>(b));
+      tmem_ld64(tDQ + 128, *reinterpret_cast<float(*)[64]>(b + 64));
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDQFree));
+      round(1, b);
+      round(2, b + 64);
+      if (DETERMINISTIC && tid == 0) {
+        bulk_wait_all<0>();
+        fence_proxy_async_global();
+        if (!*ctl.abort) red_release_gpu_add(ticket, 1);
+      }
+      __syncwarp();
+    }
+    if (tid == 0) bulk_wait_all<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool CAUSAL, bool DET, bool GQA>
+cudaError_t launch_bwd192_instance(const BwdParams& p, cudaStream_t stream, const LaunchEvents* evs) {
+  using L = Bwd192Layout;
+  auto mark = [&](int i) {
+    if (evs != nullptr && evs->ev[i] != nullptr) cudaEventRecord(evs->ev[i], stream);
+  };
+  mark(0);
+  {
+    const long rows = (long)p.BH * p.Npad;
+    const long blocks = (rows + 15) / 16;
+    bwd192_pre_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  mark(1);
+  {
+    auto kernel = bwd192_kernel<CAUSAL, DET, GQA>;
+    cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, nullptr);
+    if (e != cudaSuccess) return e;
+    const int n_heads = GQA ? p.BH / p.kv_group : p.BH;
+    kernel<<<n_heads * p.n_tiles, L::kThreads, L::kSmemBytes, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  mark(2);
+  {
+    const long blocks = ((long)p.BH * p.N * 32 + 255) / 256;  // one warp per row
+    dq192_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    mark(3);
+    return e;
+  }
+}
+
+}  // namespace attn

@@ -122,7 +122,7 @@ cudaError_t launch_fwd_fp8(const FwdParams& p, bool causal, cudaStream_t s);
 // Masked forward / backward (p.mask), d = 64 or 128 (attn_masked.cu).
 cudaError_t launch_fwd_masked(const FwdParams& p, int d, cudaStream_t s);
 cudaError_t launch_bwd_masked(const BwdParams& p, int d, bool deterministic, cudaStream_t s, const LaunchEvents* ev);
-// Grouped-query backward (p.kv_group > 1), d = 64 or 128 (attn_masked.cu).
+// Grouped-query backward (p.kv_group > 1), d = 64 or 128 (attn_bwd_gqa.cu).
 cudaError_t launch_bwd_gqa(const BwdParams& p, int d, bool causal, bool deterministic, cudaStream_t s,
                            const LaunchEvents* ev);
 struct QuantParams {
@@ -151,6 +151,9 @@ cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_par
 // Backward: preprocess, main, dQ conversion.
 cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s, const LaunchEvents* ev);
 cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, bool deterministic, cudaStream_t s, const LaunchEvents* ev);
+// d_qk = 192, d_v = 128 (attn_bwd_d192.cu); gqa: p.kv_group query heads share a K/V head.
+cudaError_t launch_bwd_d192(const BwdParams& p, bool causal, bool deterministic, bool gqa, cudaStream_t s,
+                            const LaunchEvents* ev);
 
 // Probes of the exponential paths.
 cudaError_t launch_exp2_probe(const float* x, float* out, int n, int method, cudaStream_t s);

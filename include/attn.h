@@ -26,7 +26,8 @@
  *   [B, H, N].  N is the same for queries and keys.
  * - Every device pointer must be 16-byte aligned.
  * - Supported head dims (d_qk, d_v): (64, 64), (128, 128), (192, 128) for the
- *   forward; (64, 64), (128, 128) for the backward.
+ *   forward and the backward; the masked, FP8 and split-KV entry points list
+ *   their own.
  * - B, H, N >= 1; B * H < 2^31; N < 2^24.
  * - The caller owns every buffer, including the backward workspace.  The
  *   library allocates no device memory; it keeps one device status word per
@@ -96,7 +97,13 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d_qk, int d_v, int dete
  * Backward pass: gradients of the forward with respect to q, k, v given dO.
  *   q, k, v, o, dO  bf16 [B,H,N,d] as in attn_fwd (o is the forward's output)
  *   lse             fp32 [B,H,N] from attn_fwd with the same arguments
- *   dq, dk, dv      bf16 [B,H,N,d], overwritten (not accumulated)
+ *   dq, dk, dv      bf16 [B,H,N,d], overwritten (not accumulated); dq and dk
+ *                   are d_qk wide, dv is d_v wide
+ *   (d_qk, d_v) = (192, 128) runs a kernel of its own: dV and dK (128 + 192
+ *   columns) stay in tensor memory while S^T and dP^T take turns in one
+ *   128-column region (the five products of "FlashAttention-4: Algorithm
+ *   and Kernel Pipelining Co-Design for Asymmetric Hardware Scaling",
+ *   Figure 2, unchanged).
  *   deterministic   0: dQ partial sums are added in whatever order the tiles
  *                      finish (results may differ in the last bits run to run);
  *                   1: the additions into each dQ tile happen in a fixed

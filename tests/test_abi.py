@@ -66,7 +66,10 @@ def test_workspace_sizes(lib):
     base = 2 * b * h * npad * 4 + b * h * npad * d * 4
     assert lib.attn_bwd_workspace_bytes(b, h, n, d, d, 0) == base
     assert lib.attn_bwd_workspace_bytes(b, h, n, d, d, 1) == base + 256
-    assert lib.attn_bwd_workspace_bytes(1, 1, 128, 192, 128, 0) == 0
+    # d_qk = 192: the accumulator is d_qk wide
+    assert lib.attn_bwd_workspace_bytes(1, 1, 128, 192, 128, 0) == 2 * 128 * 4 + 128 * 192 * 4
+    assert lib.attn_bwd_workspace_bytes(1, 1, 128, 192, 192, 0) == 0
+    assert lib.attn_bwd_workspace_bytes(1, 1, 128, 128, 64, 0) == 0
     assert lib.attn_bwd_workspace_bytes(0, 1, 128, 64, 64, 0) == 0
 
 
@@ -97,7 +100,10 @@ def test_backward_argument_errors(lib):
     f = lib.get_lib().attn_bwd
     p = 0x1000
     ok_ws = lib.attn_bwd_workspace_bytes(1, 2, 256, 64, 64, 0)
-    assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 192, 128, 0, 0.1, 0, p, ok_ws, None) == A.ATTN_ERR_UNSUPPORTED
+    assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 192, 192, 0, 0.1, 0, p, ok_ws, None) == A.ATTN_ERR_UNSUPPORTED
+    assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 96, 96, 0, 0.1, 0, p, ok_ws, None) == A.ATTN_ERR_UNSUPPORTED
+    # (192, 128) is supported; a workspace sized for d = 64 is too small for it
+    assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 192, 128, 0, 0.1, 0, p, ok_ws, None) == A.ATTN_ERR_WORKSPACE
     assert f(p, p, p, p, 0, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 0, p, ok_ws, None) == A.ATTN_ERR_INVALID_ARG
     assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 3, p, ok_ws, None) == A.ATTN_ERR_INVALID_ARG
     assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 0, None, ok_ws, None) == A.ATTN_ERR_WORKSPACE
@@ -237,6 +243,9 @@ def test_masked_argument_errors(lib):
     assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, None, 0.1, 0, p, ws - 1, None) == A.ATTN_ERR_WORKSPACE
     assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, 0x1001, 0.1, 0, p, ws, None) == A.ATTN_ERR_MISALIGNED
     assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 64, 64, 16, 0, None, 0.1, 2, p, ws, None) == A.ATTN_ERR_INVALID_ARG
+    ws192 = A.attn_bwd_workspace_bytes(1, 2, 300, 192, 128, 0)
+    assert ws192 > 0
+    assert b(p, p, p, p, p, p, p, p, p, 1, 2, 300, 192, 128, 16, 0, None, 0.1, 0, p, ws192, None) == A.ATTN_ERR_UNSUPPORTED
 
 
 def test_gqa_argument_errors(lib):

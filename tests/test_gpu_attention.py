@@ -81,6 +81,37 @@ def test_backward_ragged_and_small(A, d, N, causal, det):
         G.assert_grad_close(name, G.f64(got), ref)
 
 
+@pytest.mark.parametrize("N", [1, 100, 128, 257, 384, 640])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("det", [0, 1])
+def test_backward_d192_ragged_and_small(A, N, causal, det):
+    """d_qk = 192, d_v = 128 (the forward's third head shape): every gradient
+    of every head against the oracle, on one and several key tiles, a ragged
+    last tile, and two batch entries."""
+    B, H = 2, 2
+    t = G.inputs(B, H, N, 192, 128, seed=4)
+    o, lse = G.run_fwd(A, t, causal)
+    dq, dk, dv = G.run_bwd(A, t, o, lse, causal, det)
+    G.check_status(A)
+    q, k, v, do = (G.f64(t[n]) for n in ("q", "k", "v", "do"))
+    refs = ora.backward(q, k, v, do, 1.0 / math.sqrt(192), bool(causal))
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        G.assert_grad_close(name, G.f64(got), ref)
+
+
+def test_backward_d192_deterministic_is_bit_identical(A):
+    torch = G.torch_mod()
+    B, H, N = 2, 3, 1500
+    t = G.inputs(B, H, N, 192, 128, seed=5)
+    for causal in (0, 1):
+        o, lse = G.run_fwd(A, t, causal)
+        runs = [G.run_bwd(A, t, o, lse, causal, 1) for _ in range(3)]
+        G.check_status(A)
+        for r in runs[1:]:
+            for a, b in zip(runs[0], r):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 def test_multi_head_batch_layout(A):
     """Several batches and heads, with a tail: every (b, h) lands in its own slot."""
     _full_fwd_check(A, 3, 5, 200, 64, 64, True, seed=7)
@@ -205,6 +236,26 @@ def test_config5_backward_sweep(A, N, causal):
     b, h = int(rng.integers(B)), int(rng.integers(H))
     q, k, v, do = (G.f64(t[n][b, h]) for n in ("q", "k", "v", "do"))
     refs = ora.backward_head(q, k, v, do, 1.0 / math.sqrt(d), bool(causal))
+    for det in (0, 1):
+        grads = G.run_bwd(A, t, o, lse, causal, det)
+        G.check_status(A)
+        for name, got, ref in zip(("dq", "dk", "dv"), grads, refs):
+            e = G.rel_fro(G.f64(got[b, h]), ref)
+            assert e <= G.GRAD_REL, (name, det, e)
+
+
+@pytest.mark.parametrize("N", [2048, 8192])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_backward_d192_sweep(A, N, causal):
+    """d_qk = 192, d_v = 128, H = 16, B*N = 16384, both dQ modes: one seeded
+    full head (dQ, dK, dV) against the oracle."""
+    B, H = 16384 // N, 16
+    t = G.inputs(B, H, N, 192, 128)
+    o, lse = G.run_fwd(A, t, causal)
+    rng = np.random.Generator(np.random.PCG64(60 + N + causal))
+    b, h = int(rng.integers(B)), int(rng.integers(H))
+    q, k, v, do = (G.f64(t[n][b, h]) for n in ("q", "k", "v", "do"))
+    refs = ora.backward_head(q, k, v, do, 1.0 / math.sqrt(192), bool(causal))
     for det in (0, 1):
         grads = G.run_bwd(A, t, o, lse, causal, det)
         G.check_status(A)

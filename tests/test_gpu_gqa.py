@@ -1,5 +1,5 @@
 """GPU parity tests of grouped-query attention (attn_fwd_gqa,
-attn_fwd_splitkv_gqa) against the FP64 oracle.
+attn_fwd_splitkv_gqa, attn_bwd_gqa) against the FP64 oracle.
 
 Query head h of H reads K/V head h // (H / H_kv); the oracle is the plain
 attention of each query head against its K/V head (oracle/attention.py,
@@ -118,15 +118,15 @@ def _run_bwd_gqa(A, q, k, v, do, causal, det):
     return dq, dk, dv
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dqk,dv", [(64, 64), (128, 128), (192, 128)])
 @pytest.mark.parametrize("H,H_kv", [(8, 2), (6, 1), (4, 4)])
 @pytest.mark.parametrize("N", [1, 257, 640])
 @pytest.mark.parametrize("causal", [0, 1])
 @pytest.mark.parametrize("det", [0, 1])
-def test_backward_gqa(A, d, H, H_kv, N, causal, det):
+def test_backward_gqa(A, dqk, dv, H, H_kv, N, causal, det):
     B = 2
-    q, k, v = _inputs(B, H, H_kv, N, N, d, d, seed=33)
-    do = synth.decode_inputs_torch(synth.DecodeShape(B, H, N, 1, d, d), seed=34)["q"]
+    q, k, v = _inputs(B, H, H_kv, N, N, dqk, dv, seed=33)
+    do = synth.decode_inputs_torch(synth.DecodeShape(B, H, N, 1, dv, dv), seed=34)["q"]
     grads = _run_bwd_gqa(A, q, k, v, do, causal, det)
     G.check_status(A)
     refs = _oracle_bwd(G.f64(q), G.f64(k), G.f64(v), G.f64(do), bool(causal))
