@@ -12,19 +12,21 @@
 // need dV (128) + dK (192) + S^T (128) + dP^T (128) = 576 columns, over the
 // 512 an SM has.  Here S^T and dP^T take turns in one 128-column region X:
 // the compute warpgroups read S^T into registers (they keep P there for dS
-// anyway) and pack bf16 P^T into a separate 64-column region PK; once both
-// warpgroups have done so, dP^T is written over X.  dS^T is packed into PK
-// after the dV product has read P^T.  dQ_i (192 columns) spans X and PK, so
-// the next tile's S^T waits for the dQ read-out.  Totals: dV 128 + dK 192 +
-// X 128 + PK 64 = 512.
+// anyway) and pack bf16 P^T into a separate 64-column region PK.  The query
+// columns go in two halves of 64: once both warpgroups have read half m of
+// S^T, dP^T of those queries (an N = 64 product) is written over it while
+// they work on the other half.  dS^T is packed into PK after the dV product
+// has read P^T.  dQ_i (192 columns) spans X and PK; its read-out frees X
+// first, so the next tile's S^T starts before the last columns are read.
+// Totals: dV 128 + dK 192 + X 128 + PK 64 = 512.
 //
 // Shared memory: K_j 48 KiB, V_j 32 KiB, one Q_i stage 48 KiB, one dO_i stage
 // 32 KiB, dS 32 KiB, the dQ staging tile 32 KiB: 225 KiB.
 //
 // Warp roles as in bwd_kernel: warp 0 producer, warp 1 MMA issuer, warps
-// 4-11 two compute warpgroups (queries 64h .. 64h+63 each), warps 12-15 the
-// dQ warpgroup.  Atomic or deterministic dQ accumulation, causal or not,
-// grouped-query heads.
+// 4-11 two compute warpgroups (half m of the queries: warpgroup h takes
+// queries 64m+32h .. 64m+32h+31), warps 12-15 the dQ warpgroup.  Atomic or
+// deterministic dQ accumulation, causal or not, grouped-query heads.
 #pragma once
 
 #include <type_traits>
@@ -56,13 +58,14 @@ struct Bwd192Layout {
   static constexpr int kBarDOFull = 3;
   static constexpr int kBarDOEmpty = 4;
   static constexpr int kBarSFull = 5;
-  static constexpr int kBarDPFull = 6;
-  static constexpr int kBarPReady = 7;  // + half m (256 arrivals each)
-  static constexpr int kBarDSFull = 9;  // + half m
-  static constexpr int kBarDQFull = 11;
-  static constexpr int kBarDQFree = 12;  // 128 arrivals: every dQ column read
-  static constexpr int kBarAccDone = 13;
-  static constexpr int kNumBars = 14;
+  static constexpr int kBarDPFull = 6;   // + half m: dP^T of queries 64m .. 64m+63 (commit)
+  static constexpr int kBarPReady = 8;   // + half m: S^T half m read, P^T half m packed (256 arrivals)
+  static constexpr int kBarDSFull = 10;  // + half m: dS^T and dS of half m (256 arrivals)
+  static constexpr int kBarDQFull = 12;
+  static constexpr int kBarDQFreeX = 13;   // 128 arrivals: dQ columns over X read
+  static constexpr int kBarDQFreePK = 14;  // 128 arrivals: dQ columns over PK read
+  static constexpr int kBarAccDone = 15;
+  static constexpr int kNumBars = 16;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
     for (int b = 0; b < L::kNumBars; ++b) {
       uint32_t cnt = 1;
       if (b == L::kBarPReady || b == L::kBarPReady + 1 || b == L::kBarDSFull || b == L::kBarDSFull + 1) cnt = 256;
-      if (b == L::kBarDQFree) cnt = 128;
+      if (b == L::kBarDQFreeX || b == L::kBarDQFreePK) cnt = 128;
       mbar_init(bar(b), cnt);
     }
     *abort_flag = 0;
@@ -261,34 +264,34 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
     } else if (warp == 1) {
       // ============================ MMA issuer ===========================
       if (lane == 0) {
-        constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
+        constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);   // S^T
+        constexpr uint32_t kIdDP = idesc_bf16_f32(128, 64, false, false);   // dP^T, one query half
         constexpr uint32_t kIdDV = idesc_bf16_f32(128, DV, false, true);    // dV (A in tensor memory)
         constexpr uint32_t kIdDK = idesc_bf16_f32(128, DQK, false, true);   // dK (A in tensor memory)
         constexpr uint32_t kIdDQ = idesc_bf16_f32(128, DQK, true, true);    // dQ (A = dS, MN-major)
-        // C = A B^T, A and B [128 x KD] K-major in 64-column chunks kBSub apart
-        auto mma_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base, auto kd) {
+        // C = A B^T, A [128 x KD] and B [rows x KD] K-major in 64-column
+        // chunks kBSub apart
+        auto mma_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base, uint32_t id, auto kd) {
           const uint64_t da = sdesc_sw128(a_base, 16, 1024);
           const uint64_t db = sdesc_sw128(b_base, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < decltype(kd)::value / 16; ++kk) {
             const uint32_t off = (kk / 4) * kBSub + (kk % 4) * 32;
-            mma_ss(tmem + d_col, sdesc_advance(da, off), sdesc_advance(db, off), kIdS, kk > 0);
+            mma_ss(tmem + d_col, sdesc_advance(da, off), sdesc_advance(db, off), id, kk > 0);
           }
         };
         // C (+)= A[tensor memory: 128 keys x 128 queries, bf16] B, B [128
         // queries (K) x N] MN-major in 64-column chunks kBSub apart.  A's
-        // queries 64h+32m .. 64h+32m+31 sit in columns kColPK + 32h + 16m
-        // .. +15; half m takes those K steps of both warpgroups h.
+        // queries 16kk .. 16kk+15 sit in columns kColPK + 8kk .. +7; half m
+        // takes K steps kk = 4m .. 4m+3.
         auto mma_pk_half = [&](uint32_t d_col, uint32_t b_base, uint32_t id, bool acc, int m) {
           const uint64_t db = sdesc_sw128(b_base, kBSub, 1024);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int kk = 4 * hh + 2 * m + u;
-              mma_ts(tmem + d_col, tmem + L::kColPK + (kk / 4) * 32 + (kk % 4) * 8, sdesc_advance(db, kk * 2048), id,
-                     (acc || m > 0 || hh > 0 || u > 0) ? 1u : 0u);
-            }
+          for (int u = 0; u < 4; ++u) {
+            const int kk = 4 * m + u;
+            mma_ts(tmem + d_col, tmem + L::kColPK + kk * 8, sdesc_advance(db, kk * 2048), id,
+                   (acc || m > 0 || u > 0) ? 1u : 0u);
+          }
         };
         bool ok = mbar_wait(bar(L::kBarKV), 0, ctl, kB192WhereMma);
         tc_fence_after();
@@ -297,23 +300,23 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
           const uint32_t qs = sbase + L::kQOff;
           const uint32_t dos = sbase + L::kDOOff;
           if (!(ok = mbar_wait(bar(L::kBarQFull), ph, ctl, kB192WhereMma + 1))) break;
-          // X and PK hold dQ of the previous tile until it has been read
-          if (it > 0 && !(ok = mbar_wait(bar(L::kBarDQFree), ph ^ 1, ctl, kB192WhereMma + 2))) break;
+          // X holds dQ of the previous tile until its read-out got past it
+          if (it > 0 && !(ok = mbar_wait(bar(L::kBarDQFreeX), ph ^ 1, ctl, kB192WhereMma + 2))) break;
           tc_fence_after();
-          mma_kmajor(L::kColX, sbase + L::kKOff, qs, std::integral_constant<int, DQK>{});
+          mma_kmajor(L::kColX, sbase + L::kKOff, qs, kIdS, std::integral_constant<int, DQK>{});
           tc_commit(bar(L::kBarSFull));
           if (!(ok = mbar_wait(bar(L::kBarDOFull), ph, ctl, kB192WhereMma + 3))) break;
-          // dV on each half of P^T as it lands
+          // per query half m, once both warpgroups have read it from S^T and
+          // packed P^T: dV on it, then its dP^T over the S^T columns just read
 #pragma unroll
           for (int m = 0; m < 2 && ok; ++m) {
             if (!(ok = mbar_wait(bar(L::kBarPReady + m), ph, ctl, kB192WhereMma + 4))) break;
             tc_fence_after();
             mma_pk_half(L::kColDV, dos, kIdDV, it > 0, m);
+            mma_kmajor(L::kColX + 64 * m, sbase + L::kVOff, dos + m * 8192, kIdDP, std::integral_constant<int, DV>{});
+            tc_commit(bar(L::kBarDPFull + m));
           }
           if (!ok) break;
-          // both warpgroups have read all of S^T: dP^T goes over it
-          mma_kmajor(L::kColX, sbase + L::kVOff, dos, std::integral_constant<int, DV>{});
-          tc_commit(bar(L::kBarDPFull));
           tc_commit(bar(L::kBarDOEmpty));  // dO_i's last reader
 #pragma unroll
           for (int m = 0; m < 2 && ok; ++m) {
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
     const int k_glob = j * kBTile + lrow;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tX = tmem + lane_base + L::kColX;
-    const uint32_t tPK = tmem + lane_base + L::kColPK + 32 * h;
+    const uint32_t tPK = tmem + lane_base + L::kColPK + 16 * h;
     const float c_log2 = p.scale_log2;
     const bool key_dead = k_glob >= p.N;
     const float* vec = reinterpret_cast<const float*>(smem + L::kVecOff);
@@ -359,14 +362,17 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       const bool diag = CAUSAL && i == j;
       const bool mask_tile = diag || (j * kBTile + kBTile > p.N);
       // Phase 1 (S^T in X): P = 2^(S^T * scale * log2e - LSE2) for this
-      // warpgroup's 64 queries, kept in registers and packed as bf16 P^T
-      // into PK columns 32h .. 32h+31.
+      // warpgroup's queries c0 = 64m+32h .. c0+31 of each half m, kept in
+      // registers and packed as bf16 P^T into PK columns c0/2 .. c0/2+15.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, ctl, kB192WhereEw));
+      if (!ok) break;
+      // PK held dQ of the previous tile until its read-out got past it
+      if (it > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFreePK), ph ^ 1, ctl, kB192WhereEw + 2));
       if (!ok) break;
       tc_fence_after();
       float pv[64];
       auto p_chunk = [&](int m, auto masked) {
-        const int c0 = 64 * h + 32 * m;
+        const int c0 = 64 * m + 32 * h;
         float sv[32];
         tmem_ld32(tX + c0, sv);
         uint32_t pk[16];
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
           pk[q >> 1] = pack_bf16(p0, p1);
           pk[(q >> 1) + 1] = pack_bf16(p2, p3);
         }
-        tmem_st16(tPK + 16 * m, pk);
+        tmem_st16(tPK + 32 * m, pk);
       };
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
@@ -401,16 +407,18 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
         mbar_arrive(bar(L::kBarPReady + m));
       }
 
-      // Phase 2 (dP^T in X, written after both halves of P^T were ready):
-      // dS = P o (dP - D), packed as dS^T into PK (the dV product has read
-      // P^T: it was issued before dP^T) and written to shared memory as dS.
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), ph, ctl, kB192WhereEw + 1));
-      if (!ok) break;
-      tc_fence_after();
-      uint8_t* ds_row = smem + L::kDSOff + h * kBSub + (lrow >> 3) * 1024 + (lrow & 7) * 128;
+      // Phase 2 (dP^T half m in X, written once half m of S^T was read):
+      // dS = P o (dP - D), packed as dS^T into PK (the dV product of half m
+      // has read P^T there: it was issued before that dP^T) and written to
+      // shared memory as dS: query half m at m * 16 KB, key row lrow at
+      // (lrow/8)*1024 + (lrow%8)*128, 16-byte unit (q%64)/8 xor (lrow%8).
+      uint8_t* ds_row = smem + L::kDSOff + (lrow >> 3) * 1024 + (lrow & 7) * 128;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        const int c0 = 64 * h + 32 * m;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull + m), ph, ctl, kB192WhereEw + 1));
+        if (!ok) break;
+        tc_fence_after();
+        const int c0 = 64 * m + 32 * h;
         float dp[32];
         tmem_ld32(tX + c0, dp);
         uint32_t dk[16];
@@ -424,17 +432,19 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
           dk[q >> 1] = pack_bf16(ds01.x, ds01.y);
           dk[(q >> 1) + 1] = pack_bf16(ds23.x, ds23.y);
         }
-        tmem_st16(tPK + 16 * m, dk);
+        tmem_st16(tPK + 32 * m, dk);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int unit = (4 * m + u) ^ (lrow & 7);
-          *reinterpret_cast<uint4*>(ds_row + unit * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+          const int unit = (4 * h + u) ^ (lrow & 7);
+          *reinterpret_cast<uint4*>(ds_row + m * kBSub + unit * 16) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(L::kBarDSFull + m));
       }
+      if (!ok) break;
     }
     // epilogue: warpgroup h writes dV columns [64h, 64h+64) and dK columns
     // [96h, 96h+96) of its key row
@@ -471,8 +481,8 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
     // ========================== dQ warpgroup ===========================
     // Round r stages dQ columns 64r .. 64r+63 in the accumulator's [48
     // groups][128 rows][4] order and has the copy engine add them.  Columns
-    // 64 .. 191 are read before round 1 so the tensor-memory columns are
-    // freed after the first round.
+    // 0 .. 127 (over X) are read first and released to the next tile's S^T;
+    // columns 128 .. 191 (over PK) after the first round.
     const int quad = warp & 3;
     const int qrow = quad * 32 + lane;
     const int tid = threadIdx.x - 384;
@@ -519,18 +529,17 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
         }
         __syncwarp();
       };
-      {
-        float a[64];
-        tmem_ld64(tDQ, a);
-        round(0, a);
-      }
-      float b[128];
-      tmem_ld64(tDQ + 64, *reinterpret_cast<float(*)[64]>(b));
-      tmem_ld64(tDQ + 128, *reinterpret_cast<float(*)[64]>(b + 64));
+      float a[64], b[64];
+      tmem_ld64(tDQ, a);
+      tmem_ld64(tDQ + 64, b);
       tc_fence_before();
-      mbar_arrive(bar(L::kBarDQFree));
+      mbar_arrive(bar(L::kBarDQFreeX));
+      round(0, a);
+      tmem_ld64(tDQ + 128, a);
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDQFreePK));
       round(1, b);
-      round(2, b + 64);
+      round(2, a);
       if (DETERMINISTIC && tid == 0) {
         bulk_wait_all<0>();
         fence_proxy_async_global();
