@@ -48,17 +48,24 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
+def d_v(args) -> int:
+    """Head dim of V, O and dO (--dv; 0: the same as --d)."""
+    return getattr(args, "dv", 0) or args.d
+
+
 def workload(args):
-    return {"workload": f"attention fwd+bwd B={args.B} H={args.H} N={args.N} d={args.d} "
+    dims = f"d={args.d}" if d_v(args) == args.d else f"d_qk={args.d} d_v={d_v(args)}"
+    return {"workload": f"attention fwd+bwd B={args.B} H={args.H} N={args.N} {dims} "
                         f"{'causal' if args.causal else 'non-causal'} {'deterministic' if args.det else 'atomic'} dQ",
-            "B": args.B, "H": args.H, "N": args.N, "d_qk": args.d, "d_v": args.d, "causal": bool(args.causal),
-            "dq_mode": "deterministic" if args.det else "atomic", "scale": "1/sqrt(d)", "seed": 0,
+            "B": args.B, "H": args.H, "N": args.N, "d_qk": args.d, "d_v": d_v(args), "causal": bool(args.causal),
+            "dq_mode": "deterministic" if args.det else "atomic", "scale": "1/sqrt(d_qk)", "seed": 0,
             "dtype_inputs": "bf16", "l2": "256 MiB write between timed steps (outside the timed events); "
                                          "inputs 320 MiB > 129 MB L2"}
 
 
 def flops_fwd(a) -> float:
-    f = 4.0 * a.B * a.H * a.N * a.N * a.d
+    # the two forward products: 2 N^2 d_qk for S plus 2 N^2 d_v for O per head
+    f = 2.0 * a.B * a.H * a.N * a.N * (a.d + d_v(a))
     return f / 2 if a.causal else f
 
 
@@ -169,7 +176,8 @@ def recorded_traffic(kernel: str, args):
         rec = json.load(f)
     if rec.get("kernel_source_hash") != kernel_source_hash():
         return None
-    key = f"{kernel}:B{args.B}H{args.H}N{args.N}d{args.d}c{int(args.causal)}"
+    dims = f"d{args.d}" if d_v(args) == args.d else f"d{args.d}v{d_v(args)}"
+    key = f"{kernel}:B{args.B}H{args.H}N{args.N}{dims}c{int(args.causal)}"
     return rec.get("per_launch_bytes", {}).get(key)
 
 
@@ -185,15 +193,17 @@ def oracle_sample(args, rows: int = 1024):
 
     # head (0, 0) of the workload's stream: Q, K, V, dO each start after the
     # whole previous tensor (B*H*N*d draws)
-    per = args.B * args.H * args.N * args.d
-    draw = lambda start, n_rows: ora.bf16_to_f64(synth.normal_bf16_bits(0, start, (n_rows, args.d)))
-    q, k, v, do = draw(0, rows), draw(per, args.N), draw(2 * per, args.N), draw(3 * per, rows)
+    dv = d_v(args)
+    per_qk, per_v = args.B * args.H * args.N * args.d, args.B * args.H * args.N * dv
+    draw = lambda start, n_rows, d: ora.bf16_to_f64(synth.normal_bf16_bits(0, start, (n_rows, d)))
+    q, k = draw(0, rows, args.d), draw(per_qk, args.N, args.d)
+    v, do = draw(2 * per_qk, args.N, dv), draw(2 * per_qk + per_v, rows, dv)
     scale = 1.0 / math.sqrt(args.d)
     t0 = time.perf_counter()
     ora.forward_head(q, k, v, scale, bool(args.causal), np.arange(rows))
     ora.backward_head(q, k, v, do, scale, bool(args.causal))
     dt = time.perf_counter() - t0
-    fl = 3.5 * 4.0 * rows * args.N * args.d / (2 if args.causal else 1)
+    fl = 3.5 * 2.0 * rows * args.N * (args.d + dv) / (2 if args.causal else 1)
     return dt, fl, f"head (0,0): {rows} of {args.N} query rows x {args.N} keys, forward + backward, FP64"
 
 
@@ -225,21 +235,21 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     A.get_lib()
-    B, H, N, d = args.B, args.H, args.N, args.d
+    B, H, N, d, dvh = args.B, args.H, args.N, args.d, d_v(args)
     scale = 1.0 / math.sqrt(d)
-    t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, d, d), seed=0, device=dev)
+    t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, d, dvh), seed=0, device=dev)
     q, k, v, do = t["q"], t["k"], t["v"], t["do"]
     o = torch.empty_like(v)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    nws = A.attn_bwd_workspace_bytes(B, H, N, d, d, args.det)
+    nws = A.attn_bwd_workspace_bytes(B, H, N, d, dvh, args.det)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        A.attn_fwd(q, k, v, o, lse, B, H, N, d, d, args.causal, scale, stream)
-        A.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, d, args.causal, scale, args.det, ws, nws, stream)
+        A.attn_fwd(q, k, v, o, lse, B, H, N, d, dvh, args.causal, scale, stream)
+        A.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, dvh, args.causal, scale, args.det, ws, nws, stream)
 
     for _ in range(args.warmup):
         step()
@@ -295,7 +305,7 @@ def run_ours(args, world, rank, local):
     pairs_in = [(flat(dst), flat(src)) for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo))]
     pairs_out = [(flat(dst), flat(src)) for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv))]
     dev_t = [flat(x) for x in (q, k, v, o, do, lse, dq, dk, dv)]
-    cws = A.attn_bwd_workspace_bytes(1, hc, N, d, d, args.det)
+    cws = A.attn_bwd_workspace_bytes(1, hc, N, d, dvh, args.det)
     n_cs = max(1, min(args.e2e_streams, n_chunks))  # compute streams, groups dealt round-robin
     cwsb = [torch.empty(cws, dtype=torch.uint8, device=dev) for _ in range(n_cs)]
     s_comp = [stream] + [torch.cuda.Stream(dev) for _ in range(n_cs - 1)]
@@ -324,8 +334,8 @@ def run_ours(args, world, rank, local):
             if not first[0]:
                 cs.wait_event(ev_out[c])  # the previous step's results of group c are out
             cq, ck, cv, co, cdo, clse, cdq, cdk, cdv = (x[sl] for x in dev_t)
-            A.attn_fwd(cq, ck, cv, co, clse, 1, hc, N, d, d, args.causal, scale, cs)
-            A.attn_bwd(cq, ck, cv, co, cdo, clse, cdq, cdk, cdv, 1, hc, N, d, d, args.causal, scale, args.det,
+            A.attn_fwd(cq, ck, cv, co, clse, 1, hc, N, d, dvh, args.causal, scale, cs)
+            A.attn_bwd(cq, ck, cv, co, cdo, clse, cdq, cdk, cdv, 1, hc, N, d, dvh, args.causal, scale, args.det,
                        cwsb[c % n_cs], cws, cs)
             ev_done[c].record(cs)
             s_out.wait_event(ev_done[c])
@@ -540,7 +550,8 @@ def main(argv=None):
     ap.add_argument("--B", type=int, default=1)
     ap.add_argument("--H", type=int, default=16)
     ap.add_argument("--N", type=int, default=16384)
-    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--d", type=int, default=128, help="head dim of Q and K (d_qk)")
+    ap.add_argument("--dv", type=int, default=0, help="head dim of V, O and dO (0: the same as --d)")
     ap.add_argument("--causal", type=int, default=0)
     ap.add_argument("--det", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

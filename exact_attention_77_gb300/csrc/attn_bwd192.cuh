@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
           const int qh = head_q(qi);
           const uint32_t ph = (it & 1) ^ 1;
           if (!mbar_wait(bar(L::kBarQEmpty), ph, ctl, kB192WhereProd)) break;
+          ATTN_TRACE_AT(blockIdx.x, it, 25);
           mbar_arrive_expect_tx(bar(L::kBarQFull), L::kQKBytes + L::kVecBytes);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
@@ -254,6 +255,18 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
           for (int c = 0; c < DV / 64; ++c)
             tma_load_3d(sbase + L::kDOOff + c * kBSub, &p.tm_do, c * 64, i * kBTile, qh, bar(L::kBarDOFull));
           issued_do = it + 1;
+          // With one Q stage the next Q_i load sits on the critical path (it
+          // starts when this tile's dK product is done).  In deterministic
+          // mode, fetching its tiles into L2 a whole tile ahead measured 3-4 %
+          // faster on GB300; with atomic dQ 3 % slower (there the load waits
+          // behind the dQ reduce-adds, not on DRAM), so only there.
+          if (DETERMINISTIC && it + 1 < n_it) {
+            const int qn = i_next(qi);
+#pragma unroll
+            for (int c = 0; c < DQK / 64; ++c) tma_prefetch_l2_3d(&p.tm_q, c * 64, tile_i(qn) * kBTile, head_q(qn));
+#pragma unroll
+            for (int c = 0; c < DV / 64; ++c) tma_prefetch_l2_3d(&p.tm_do, c * 64, tile_i(qn) * kBTile, head_q(qn));
+          }
         }
         // loads in flight land before the CTA exits (one stage per ring)
         mbar_wait_drain(bar(L::kBarKV), 0, p.timeout_ns);
@@ -300,17 +313,21 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
           const uint32_t qs = sbase + L::kQOff;
           const uint32_t dos = sbase + L::kDOOff;
           if (!(ok = mbar_wait(bar(L::kBarQFull), ph, ctl, kB192WhereMma + 1))) break;
+          ATTN_TRACE_AT(blockIdx.x, it, 0);
           // X holds dQ of the previous tile until its read-out got past it
           if (it > 0 && !(ok = mbar_wait(bar(L::kBarDQFreeX), ph ^ 1, ctl, kB192WhereMma + 2))) break;
+          ATTN_TRACE_AT(blockIdx.x, it, 1);
           tc_fence_after();
           mma_kmajor(L::kColX, sbase + L::kKOff, qs, kIdS, std::integral_constant<int, DQK>{});
           tc_commit(bar(L::kBarSFull));
           if (!(ok = mbar_wait(bar(L::kBarDOFull), ph, ctl, kB192WhereMma + 3))) break;
+          ATTN_TRACE_AT(blockIdx.x, it, 3);
           // per query half m, once both warpgroups have read it from S^T and
           // packed P^T: dV on it, then its dP^T over the S^T columns just read
 #pragma unroll
           for (int m = 0; m < 2 && ok; ++m) {
             if (!(ok = mbar_wait(bar(L::kBarPReady + m), ph, ctl, kB192WhereMma + 4))) break;
+            ATTN_TRACE_AT(blockIdx.x, it, 4 + 2 * m);
             tc_fence_after();
             mma_pk_half(L::kColDV, dos, kIdDV, it > 0, m);
             mma_kmajor(L::kColX + 64 * m, sbase + L::kVOff, dos + m * 8192, kIdDP, std::integral_constant<int, DV>{});
@@ -321,6 +338,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
 #pragma unroll
           for (int m = 0; m < 2 && ok; ++m) {
             if (!(ok = mbar_wait(bar(L::kBarDSFull + m), ph, ctl, kB192WhereMma + 6))) break;
+            ATTN_TRACE_AT(blockIdx.x, it, 8 + m);
             tc_fence_after();
             mma_pk_half(L::kColDK, qs, kIdDK, it > 0, m);
           }
@@ -334,18 +352,46 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
               mma_ss(tmem + L::kColDQ, sdesc_advance(da, kk * 2048), sdesc_advance(db, kk * 2048), kIdDQ, kk > 0);
           }
           tc_commit(bar(L::kBarDQFull));
+          ATTN_TRACE_AT(blockIdx.x, it, 10);
         }
         tc_commit(bar(L::kBarAccDone));
         mbar_wait_drain(bar(L::kBarAccDone), 0, p.timeout_ns);
       }
       __syncwarp();
     }
+#ifdef ATTN_TRACE
+    else if (warp == 2) {
+      // debug only: completion times of the products, seen by polling
+      if (lane == 0 && blockIdx.x < kTraceCtas) {
+        bool live = true;
+        auto seen = [&](uint32_t b, uint32_t par) {
+          for (int i = 0; live && i < (1 << 22); ++i)
+            if (mbar_test(b, par)) return;
+          live = false;
+        };
+        for (int it = 0; live && it < n_it && it < kTraceIters; ++it) {
+          seen(bar(L::kBarSFull), it & 1);
+          ATTN_TRACE_AT(blockIdx.x, it, 27);
+          seen(bar(L::kBarDPFull), it & 1);
+          ATTN_TRACE_AT(blockIdx.x, it, 28);
+          seen(bar(L::kBarDPFull + 1), it & 1);
+          ATTN_TRACE_AT(blockIdx.x, it, 29);
+          seen(bar(L::kBarQEmpty), it & 1);
+          ATTN_TRACE_AT(blockIdx.x, it, 30);
+          seen(bar(L::kBarDQFull), it & 1);
+          ATTN_TRACE_AT(blockIdx.x, it, 31);
+        }
+      }
+      __syncwarp();
+    }
+#endif
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kComputeRegs));
     // ================= two compute warpgroups (h = 0, 1) =================
     const int h = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int lrow = quad * 32 + lane;  // tensor-memory lane: key row
+    const int tid = threadIdx.x - 128 - 128 * h;  // 0..127 within the warpgroup
     const int k_glob = j * kBTile + lrow;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tX = tmem + lane_base + L::kColX;
@@ -366,9 +412,11 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       // registers and packed as bf16 P^T into PK columns c0/2 .. c0/2+15.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, ctl, kB192WhereEw));
       if (!ok) break;
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 11 + h);
       // PK held dQ of the previous tile until its read-out got past it
       if (it > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFreePK), ph ^ 1, ctl, kB192WhereEw + 2));
       if (!ok) break;
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 13 + h);
       tc_fence_after();
       float pv[64];
       auto p_chunk = [&](int m, auto masked) {
@@ -406,6 +454,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
         tc_fence_before();
         mbar_arrive(bar(L::kBarPReady + m));
       }
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 15 + h);
 
       // Phase 2 (dP^T half m in X, written once half m of S^T was read):
       // dS = P o (dP - D), packed as dS^T into PK (the dV product of half m
@@ -417,6 +466,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       for (int m = 0; m < 2; ++m) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull + m), ph, ctl, kB192WhereEw + 1));
         if (!ok) break;
+        if (tid == 0 && m == 0) ATTN_TRACE_AT(blockIdx.x, it, 17 + h);
         tc_fence_after();
         const int c0 = 64 * m + 32 * h;
         float dp[32];
@@ -445,6 +495,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
         mbar_arrive(bar(L::kBarDSFull + m));
       }
       if (!ok) break;
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 19 + h);
     }
     // epilogue: warpgroup h writes dV columns [64h, 64h+64) and dK columns
     // [96h, 96h+96) of its key row
@@ -494,6 +545,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       const int qh = head_q(qi);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kB192WhereDq));
       if (!ok) break;
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 21);
       tc_fence_after();
       float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(DQK * kBTile);
       int* ticket = DETERMINISTIC ? p.tickets + (size_t)qh * p.n_tiles + i : nullptr;
@@ -534,12 +586,15 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       tmem_ld64(tDQ + 64, b);
       tc_fence_before();
       mbar_arrive(bar(L::kBarDQFreeX));
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 22);
       round(0, a);
       tmem_ld64(tDQ + 128, a);
       tc_fence_before();
       mbar_arrive(bar(L::kBarDQFreePK));
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 23);
       round(1, b);
       round(2, a);
+      if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 24);
       if (DETERMINISTIC && tid == 0) {
         bulk_wait_all<0>();
         fence_proxy_async_global();

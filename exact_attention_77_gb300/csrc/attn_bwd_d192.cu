@@ -21,3 +21,10 @@ cudaError_t launch_bwd_d192(const BwdParams& p, bool causal, bool deterministic,
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TRACE
+// Debug builds only: the phase-trace stamps of this translation unit's kernels.
+extern "C" int attn_debug_trace_read_d192(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, attn::g_attn_trace, bytes) == cudaSuccess ? 0 : 5;
+}
+#endif

@@ -44,9 +44,15 @@ def test_flop_convention():
     assert bench.flops_fwd(a) == 4 * 16 * 16384 ** 2 * 128
     a.causal = 1
     assert bench.flops_fwd(a) == 2 * 16 * 16384 ** 2 * 128
+    # d_qk != d_v: the S product counts d_qk, the O product d_v
+    b = type("A", (), dict(B=1, H=16, N=4096, d=192, dv=128, causal=0))()
+    assert bench.flops_fwd(b) == 2 * 16 * 4096 ** 2 * (192 + 128)
 
 
 def test_oracle_sample_runs_small():
     a = type("A", (), dict(B=1, H=1, N=256, d=64, causal=0))()
     dt, fl, desc = bench.oracle_sample(a, rows=64)
     assert dt > 0 and fl == 3.5 * 4 * 64 * 256 * 64 and "64 of 256" in desc
+    b = type("A", (), dict(B=1, H=1, N=256, d=192, dv=128, causal=1))()
+    dt, fl, desc = bench.oracle_sample(b, rows=64)
+    assert dt > 0 and fl == 3.5 * 2 * 64 * 256 * (192 + 128) / 2
