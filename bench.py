@@ -157,13 +157,40 @@ def measured_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source without its // and /* */ comments (string and character
+    literals kept as they are), so an edit to comments alone leaves the
+    source hash unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources' code (comments excluded): the committed DRAM
+    counters stay valid while it is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_77_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + strip_c_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

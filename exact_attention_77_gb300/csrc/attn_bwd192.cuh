@@ -2,8 +2,8 @@
 //
 // The same graph of five products and two elementwise steps as bwd_kernel
 // ("FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
-// Asymmetric Hardware Scaling", Figure 2 and Table 3), for the head shape of
-// the forward's third configuration (d_qk = 192, d_v = 128):
+// Asymmetric Hardware Scaling", Figure 2 and Table 3), for the head shape
+// d_qk = 192, d_v = 128 that the same page's Figure 5 measures its forward on:
 //     S^T  = K_j Q_i^T   (K = 192)        dP^T = V_j dO_i^T   (K = 128)
 //     dV  += P^T dO_i    (N = 128)        dK  += dS^T Q_i     (N = 192)
 //     dQ_i = dS K_j      (N = 192)

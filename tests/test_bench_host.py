@@ -56,3 +56,10 @@ def test_oracle_sample_runs_small():
     b = type("A", (), dict(B=1, H=1, N=256, d=192, dv=128, causal=1))()
     dt, fl, desc = bench.oracle_sample(b, rows=64)
     assert dt > 0 and fl == 3.5 * 2 * 64 * 256 * (192 + 128) / 2
+
+
+def test_source_hash_ignores_comments_only():
+    src = 'const char* s = "a // b /* c */";  // note\nint x = 1; /* block\n comment */ int y = \'/\';\n'
+    assert bench.strip_c_comments(src) == 'const char* s = "a // b /* c */";  \nint x = 1;  int y = \'/\';\n'
+    assert bench.strip_c_comments("a = 1; // x") == bench.strip_c_comments("a = 1; // y")
+    assert bench.strip_c_comments("a = 1;") != bench.strip_c_comments("a = 2;")
