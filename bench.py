@@ -209,22 +209,31 @@ def recorded_traffic(kernel: str, args):
 
 
 # ---------------------------------------------------------- CPU oracle
+def oracle_inputs(args, rows: int):
+    """FP64 values of head (0, 0) of the workload's seeded stream: the first
+    ``rows`` query rows of Q and dO, every row of K and V.  Q, K, V, dO each
+    start after the whole previous tensor (B*H*N*d draws)."""
+    import synth
+    from oracle import attention as ora
+
+    dv = d_v(args)
+    per_qk, per_v = args.B * args.H * args.N * args.d, args.B * args.H * args.N * dv
+    draw = lambda start, n_rows, d: ora.bf16_to_f64(synth.normal_bf16_bits(0, start, (n_rows, d)))
+    q, k = draw(0, rows, args.d), draw(per_qk, args.N, args.d)
+    v, do = draw(2 * per_qk, args.N, dv), draw(2 * per_qk + per_v, rows, dv)
+    return q, k, v, do
+
+
 def oracle_sample(args, rows: int = 1024):
     """The oracle's forward and backward for ``rows`` query rows of head (0, 0)
     against all N keys (non-causal rows are independent, so this is exactly
     those rows' share of the workload).  Returns (seconds, flops, description)."""
     import numpy as np
 
-    import synth
     from oracle import attention as ora
 
-    # head (0, 0) of the workload's stream: Q, K, V, dO each start after the
-    # whole previous tensor (B*H*N*d draws)
     dv = d_v(args)
-    per_qk, per_v = args.B * args.H * args.N * args.d, args.B * args.H * args.N * dv
-    draw = lambda start, n_rows, d: ora.bf16_to_f64(synth.normal_bf16_bits(0, start, (n_rows, d)))
-    q, k = draw(0, rows, args.d), draw(per_qk, args.N, args.d)
-    v, do = draw(2 * per_qk, args.N, dv), draw(2 * per_qk + per_v, rows, dv)
+    q, k, v, do = oracle_inputs(args, rows)
     scale = 1.0 / math.sqrt(args.d)
     t0 = time.perf_counter()
     ora.forward_head(q, k, v, scale, bool(args.causal), np.arange(rows))

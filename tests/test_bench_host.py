@@ -4,6 +4,7 @@ import math
 import os
 import socket
 
+import numpy as np
 import pytest
 
 import bench
@@ -63,3 +64,18 @@ def test_source_hash_ignores_comments_only():
     assert bench.strip_c_comments(src) == 'const char* s = "a // b /* c */";  \nint x = 1;  int y = \'/\';\n'
     assert bench.strip_c_comments("a = 1; // x") == bench.strip_c_comments("a = 1; // y")
     assert bench.strip_c_comments("a = 1;") != bench.strip_c_comments("a = 2;")
+
+
+@pytest.mark.parametrize("d,dv", [(64, 64), (192, 128)])
+def test_oracle_sample_draws_head_zero_of_the_workload(d, dv):
+    """The CPU baseline's sample is head (0, 0) of the same seeded tensors the
+    GPU step runs on."""
+    import synth
+    from oracle import attention as ora
+
+    a = type("A", (), dict(B=2, H=3, N=130, d=d, dv=dv, causal=0))()
+    q, k, v, do = bench.oracle_inputs(a, rows=17)
+    full = synth.attention_inputs(synth.AttentionShape(2, 3, 130, d, dv), seed=0)
+    f = {n: ora.bf16_to_f64(full[n])[0, 0] for n in ("q", "k", "v", "do")}
+    assert np.array_equal(q, f["q"][:17]) and np.array_equal(k, f["k"])
+    assert np.array_equal(v, f["v"]) and np.array_equal(do, f["do"][:17])
