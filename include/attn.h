@@ -359,6 +359,8 @@ int attn_set_bwd_pair(int enable);
  * N <= 2048, and for N <= 4096 in atomic mode.  Results meet the same
  * tolerances either way; deterministic mode is bit-identical run to run with
  * either kernel (the two may differ from each other in the last bits).
+ * Applies to d_qk = d_v = 64 and 128 without grouped-query heads or masks;
+ * the other backward calls always run one CTA per unit.
  * Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
  */
 int attn_set_bwd_persist(int mode);
