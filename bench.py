@@ -16,13 +16,16 @@ fraction of the measured dense BF16 peak.
 --impl reference times the FP64 CPU oracle on the host cores (a bounded sample
 of the same workload per step).
 
-  python bench.py --case fp8|splitkv|masked [--B --H --N ...]
+  python bench.py --case fp8|splitkv|masked|exp2|detsched [--B --H --N ...]
 
 times one of the library's other paths instead (one GPU; a JSON line with its
 own fields; no contract line): the FP8 quantiser + FP8 forward, the split-KV
 decode forward (--Nq queries against --Nk keys, the heuristic's ranges), or
 the masked forward + backward (--window-left / --window-right, --block-density
-for a seeded random block map).  Under torchrun every rank runs the same
+for a seeded random block map), or the exponential paths' accuracy (the
+experiment of Table 2 of the FlashAttention-4 paper) and throughput per SM
+per clock, or the deterministic backward under each unit order (detsched).
+Under torchrun every rank runs the same
 workload on its own GPU (independent replicas: no data exchange), timing is
 bracketed by barriers and the slowest rank's time is used.
 """
@@ -147,6 +150,25 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def roofline_peak(peaks: dict, clk: dict):
+    """Denominator of the roofline fractions: the burst bf16 peak (cuBLAS timed
+    alone, at full clock), unless the clock record of the timed region shows
+    the power cap acting, in which case the sustained (power-capped) peak."""
+    if "sw_power_cap" in (clk.get("reasons") or []):
+        return peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]), \
+            "bf16_tflops_sustained (power cap active during the timed region)"
+    return peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]), "bf16_tflops (burst; no power cap in the timed region)"
+
+
+def gpu_uuid(torch, dev):
+    """nvidia-smi id of the torch device (its UUID), or None."""
+    try:
+        g = str(torch.cuda.get_device_properties(dev).uuid)
+        return g if g.startswith("GPU-") else "GPU-" + g
+    except Exception:
+        return None
 
 
 def measured_peaks():
@@ -294,12 +316,7 @@ def run_ours(args, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {A.status_string(st)} at {where}")
 
-    gpu_id = None
-    try:
-        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
-        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
-    except Exception:
-        gpu_id = None
+    gpu_id = gpu_uuid(torch, dev)
     clocks = ClockSampler(gpu_id)
     time.sleep(0.5)
     barrier(world)
@@ -320,6 +337,34 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status after timed steps: {A.status_string(st)} at {where}")
     step_ms = sum(a.elapsed_time(b) for a, b in evs)
     total_ms = max_over_ranks(step_ms, world, dev)
+
+    # sustained leg: the same step back to back for >= --sustain-seconds with
+    # clocks sampled, to show whether the rates hold under the power limit
+    # (inputs and outputs are 320 MiB > 129 MB of L2, so no flush between steps)
+    sustained = None
+    if args.sustain_seconds > 0:
+        n_sus = max(args.steps, int(math.ceil(args.sustain_seconds / max(step_ms / args.steps / 1e3, 1e-6))))
+        clocks_s = ClockSampler(gpu_id)
+        time.sleep(0.5)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        A.attn_profile_start()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n_sus):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        prof_s = A.attn_profile_stop()
+        barrier(world)
+        clk_s = clocks_s.stop()
+        sus_ms = max_over_ranks(s0.elapsed_time(s1), world, dev)
+        f1 = flops_fwd(args)
+        sustained = {
+            "steps": n_sus, "seconds": sus_ms / 1e3, "value": world * 3.5 * f1 * n_sus / (sus_ms / 1e3) / 1e12,
+            "forward_tflops": f1 * prof_s["launches_fwd"] / (prof_s["ms_fwd"] / 1e3) / 1e12,
+            "backward_main_tflops": 2.5 * f1 * prof_s["launches_bwd_main"] / (prof_s["ms_bwd_main"] / 1e3) / 1e12,
+            "clocks": clk_s, "l2": "no flush: 320 MiB of inputs and outputs per step > 129 MB L2"}
 
     # end to end through the public API: pinned host buffers in, results out.
     # Every (b, h) is independent, so the step runs as n_chunks groups of
@@ -415,19 +460,16 @@ def run_ours(args, world, rank, local):
         ach = fl / (avg / 1e3) / 1e12 if avg > 0 else None
         per_kernel[name] = {"launches": n, "avg_ms": avg, "achieved_tflops": ach}
     dom = max(kernels, key=lambda n: kernels[n][0])
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    ach = per_kernel[dom]["achieved_tflops"]
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak if ach else None, "traffic": recorded_traffic(dom, args),
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a multi-kernel step)",
-                "frac_of_nominal_2250": ach / 2250.0 if ach else None}
-    fwd_ach = per_kernel["attn_fwd_kernel"]["achieved_tflops"]
-    roofline_fwd = {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": fwd_ach,
-                    "peak": peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]), "unit": "TFLOP/s",
-                    "frac": fwd_ach / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) if fwd_ach else None,
-                    "peak_source": f"{peak_src} bf16_tflops (burst)",
-                    "frac_of_nominal_2250": fwd_ach / 2250.0 if fwd_ach else None,
-                    "traffic": recorded_traffic("attn_fwd_kernel", args)}
+    peak, peak_note = roofline_peak(peaks, clk)
+
+    def roof(name):
+        a = per_kernel[name]["achieved_tflops"]
+        return {"bound": "tensor", "kernel": name, "achieved": a, "peak": peak, "unit": "TFLOP/s",
+                "frac": a / peak if a else None, "traffic": recorded_traffic(name, args),
+                "peak_source": f"{peak_src} {peak_note}", "frac_of_nominal_2250": a / 2250.0 if a else None}
+
+    roofline = roof(dom)
+    roofline_fwd = roof("attn_fwd_kernel")
     launches = prof["launches_fwd"] + prof["launches_bwd_pre"] + prof["launches_bwd_main"] + prof["launches_bwd_convert"]
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -435,9 +477,9 @@ def run_ours(args, world, rank, local):
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16; splitmix64 + Box-Muller, seed 0)",
         "config": dict(workload(args), parallelism=f"replicas{world}" if world > 1 else "single"),
         "roofline": roofline, "roofline_fwd": roofline_fwd, "kernels": per_kernel,
-        "breakdown_tflops": {"forward": fwd_ach, "backward_main": per_kernel["attn_bwd_main_kernel"]["achieved_tflops"],
+        "breakdown_tflops": {"forward": per_kernel["attn_fwd_kernel"]["achieved_tflops"], "backward_main": per_kernel["attn_bwd_main_kernel"]["achieved_tflops"],
                              "backward_incl_pre_convert": 2.5 * f_fwd / ((prof["ms_bwd_pre"] + prof["ms_bwd_main"] + prof["ms_bwd_convert"]) / max(prof["launches_bwd_main"], 1) / 1e3) / 1e12 if prof["launches_bwd_main"] else None},
-        "clocks": clk, "gpu_launches": launches,
+        "clocks": clk, "gpu_launches": launches, "sustained": sustained,
         "e2e": {"value": world * f_step / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "head_groups": n_chunks,
                 "compute_streams": n_cs},
@@ -472,6 +514,111 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------- other library paths
+def run_exp2_case(args, A, torch, dev, out):
+    """The exponential paths of the forward measured on the device: the
+    relative error of 2^x on 4M uniform FP32 inputs on [0, 1) against FP64
+    (the experiment of "FlashAttention-4 ...", Table 2; BF16 columns after
+    rounding to bfloat16), and the throughput of each path in exponentials
+    per SM per clock, from CUDA events and the SM clock sampled while the
+    throughput kernel runs."""
+    import numpy as np
+
+    names = {0: "mufu", 3: "degree3", 4: "degree4", 5: "degree5"}
+    rng = np.random.Generator(np.random.PCG64(0))
+    f = rng.random(4_000_000).astype(np.float32)
+    f = f[f < 1.0]
+    x = torch.from_numpy(f).to(dev)
+    y = torch.empty_like(x)
+    exact = np.exp2(f.astype(np.float64))
+
+    def bf16(v):
+        b = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32)
+        r = ((b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)) << np.uint32(16)
+        return r.view(np.float32).astype(np.float64)
+
+    acc = {}
+    for m, name in names.items():
+        A.attn_exp2_probe(x, y, x.numel(), m)
+        torch.cuda.synchronize(dev)
+        v = y.cpu().numpy()
+        r32 = np.abs(v.astype(np.float64) - exact) / exact
+        rbf = np.abs(bf16(v) - exact) / exact
+        acc[name] = {"fp32_max": float(r32.max()), "fp32_mean": float(r32.mean()),
+                     "bf16_max": float(rbf.max()), "bf16_mean": float(rbf.mean())}
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = sms * 8, 20000
+    sink = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    thr = {}
+    for m, name in names.items():
+        A.attn_exp2_throughput(sink, blocks, 100, m)  # warm-up
+        torch.cuda.synchronize(dev)
+        clocks = ClockSampler(gpu_uuid(torch, dev))
+        time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        reps = 0
+        t_end = time.perf_counter() + 1.5
+        while time.perf_counter() < t_end:
+            A.attn_exp2_throughput(sink, blocks, iters, m)
+            reps += 1
+            if reps % 4 == 0:
+                torch.cuda.synchronize(dev)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        sec = e0.elapsed_time(e1) / 1e3
+        n_exp = reps * blocks * 256 * iters * 8
+        mhz = clk.get("sm_mhz") or 0.0
+        thr[name] = {"exp_per_s": n_exp / sec, "sm_mhz_median": mhz, "reasons": clk.get("reasons"),
+                     "exp_per_clk_per_sm": n_exp / sec / (mhz * 1e6) / sms if mhz else None}
+    out.update({"config": {"inputs": "4M uniform FP32 on [0,1), PCG64 seed 0", "throughput_grid": f"{blocks}x256",
+                           "chained_exponentials_per_thread": iters * 8}, "accuracy": acc, "throughput": thr})
+
+
+def run_detsched_case(args, A, torch, dev, out):
+    """The deterministic backward under each unit order of attn_set_det_schedule
+    (head groups x ascending / descending key tiles), next to the atomic mode,
+    on the --B --H --N --d --causal workload: main-kernel time from the
+    library's per-kernel events, L2 flushed before each call, median of --steps."""
+    import synth
+
+    B, H, N, d = args.B, args.H, args.N, args.d
+    t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, d, d), seed=0, device=dev)
+    o = torch.empty_like(t["v"])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    scale = 1.0 / math.sqrt(d)
+    A.attn_fwd(t["q"], t["k"], t["v"], o, lse, B, H, N, d, d, args.causal, scale)
+    nb = A.attn_bwd_workspace_bytes(B, H, N, d, d, 1)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    fl = 2.5 * flops_fwd(args)
+
+    def main_ms(det):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i & 0xFF)
+            A.attn_profile_start()
+            A.attn_bwd(t["q"], t["k"], t["v"], o, t["do"], lse, dq, dk, dv, B, H, N, d, d, args.causal, scale, det,
+                       ws, nb)
+            prof = A.attn_profile_stop()
+            if i >= args.warmup:
+                ts.append(prof["ms_bwd_main"])
+        return statistics.median(ts)
+
+    rows = {"atomic": main_ms(0)}
+    groups = [g for g in (1, 2, 4, 8) if g < B * H] + [0]
+    for desc in (0, 1):
+        for g in groups:
+            A.attn_set_det_schedule(g, desc)
+            rows[f"group={g or 'all'} {'desc' if desc else 'asc'}"] = main_ms(1)
+    A.attn_set_det_schedule(0, 0)
+    out.update({"config": {"B": B, "H": H, "N": N, "d": d, "causal": bool(args.causal)},
+                "backward_main_ms": rows,
+                "backward_main_tflops": {k: fl / v / 1e9 for k, v in rows.items()},
+                "note": "deterministic backward main kernel per unit order; group = heads per key-tile-major group"})
+
+
 def run_case(args):
     """Time the FP8, split-KV or masked path (CUDA events, L2 flushed before
     each timed call, median of --steps after --warmup)."""
@@ -504,6 +651,10 @@ def run_case(args):
         return statistics.median(ts)
 
     out = {"case": args.case, "steps": args.steps, "warmup": args.warmup, "data": "synthetic (seeded N(0,1) bf16)"}
+    if args.case in ("exp2", "detsched"):
+        (run_exp2_case if args.case == "exp2" else run_detsched_case)(args, A, torch, dev, out)
+        print(json.dumps(out), flush=True)
+        return
     if args.case == "fp8":
         t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, d, d), seed=0, with_do=False, device=dev)
         nt = (N + 127) // 128
@@ -591,10 +742,12 @@ def main(argv=None):
     ap.add_argument("--causal", type=int, default=0)
     ap.add_argument("--det", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustain-seconds", type=float, default=2.0,
+                    help="length of the back-to-back sustained leg (0: skip it)")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="head groups pipelined through host copies and compute in the e2e leg")
     ap.add_argument("--e2e-streams", type=int, default=3, help="compute streams the e2e leg deals its groups to")
-    ap.add_argument("--case", choices=("step", "fp8", "splitkv", "masked"), default="step",
+    ap.add_argument("--case", choices=("step", "fp8", "splitkv", "masked", "exp2", "detsched"), default="step",
                     help="step: the benchmark contract; others time the library's other paths")
     ap.add_argument("--Nq", type=int, default=1)
     ap.add_argument("--Nk", type=int, default=16384)

@@ -40,6 +40,8 @@ _SIGS = {
     "attn_set_rescale_threshold": (_I, [_F]),
     "attn_set_bwd_pair": (_I, [_I]),
     "attn_set_bwd_persist": (_I, [_I]),
+    "attn_set_exp_poly": (_I, [_I]),
+    "attn_set_det_schedule": (_I, [_I, _I]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t, _P]),
@@ -290,6 +292,14 @@ def attn_set_bwd_pair(enable: int):
 
 def attn_set_bwd_persist(mode: int):
     _check(get_lib().attn_set_bwd_persist(int(mode)))
+
+
+def attn_set_exp_poly(enable: int):
+    _check(get_lib().attn_set_exp_poly(int(enable)))
+
+
+def attn_set_det_schedule(head_group: int, descending: int):
+    _check(get_lib().attn_set_det_schedule(int(head_group), int(descending)))
 
 
 def attn_selftest_wait_timeout(timeout_us: int, stream=None):

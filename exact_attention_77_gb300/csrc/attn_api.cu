@@ -29,6 +29,8 @@ struct Settings {
   int fwd_persist = -1;  // -1: by sequence length; 0 / 1 forces
   int bwd_pair = 0;      // 1: d = 128 backward on CTA pairs
   int bwd_persist = -1;  // -1: by sequence length; 0 / 1 forces persistent backward CTAs
+  int det_group = 0;     // deterministic backward: heads per group of the unit order (0: all heads)
+  int det_desc = 0;      // deterministic backward: 1 = key tiles from the last down
   int merge_pdl = 1;     // 1: split-KV merge as a programmatic dependent launch
   float fp8_tau = 4.f;   // FP8 forward: rescale threshold (P stored as e4m3(2^(8 - tau) P))
   float tau = 8.0f;
@@ -82,6 +84,11 @@ Settings settings() {
     if (const char* e = getenv("ATTN_BWD_PAIR")) g_settings.bwd_pair = atoi(e) != 0;
     if (const char* e = getenv("ATTN_BWD_PERSIST")) g_settings.bwd_persist = atoi(e);
     if (const char* e = getenv("ATTN_MERGE_PDL")) g_settings.merge_pdl = atoi(e) != 0;
+    if (const char* e = getenv("ATTN_DET_GROUP")) {
+      const int v = atoi(e);
+      if (v >= 0) g_settings.det_group = v;
+    }
+    if (const char* e = getenv("ATTN_DET_DESC")) g_settings.det_desc = atoi(e) != 0;
     if (const char* e = getenv("ATTN_FP8_TAU")) {
       const int v = atoi(e);
       if (v >= 0 && v <= 8) g_settings.fp8_tau = (float)v;
@@ -334,6 +341,23 @@ int attn_set_bwd_persist(int mode) {
   return ATTN_OK;
 }
 
+int attn_set_det_schedule(int head_group, int descending) {
+  if (head_group < 0 || (descending != 0 && descending != 1)) return ATTN_ERR_INVALID_ARG;
+  settings();
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_settings.det_group = head_group;
+  g_settings.det_desc = descending;
+  return ATTN_OK;
+}
+
+int attn_set_exp_poly(int enable) {
+  if (enable != 0 && enable != 1) return ATTN_ERR_INVALID_ARG;
+  settings();
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_settings.fwd_poly = enable;
+  return ATTN_OK;
+}
+
 int attn_set_rescale_threshold(float tau) {
   if (!isfinite(tau) || tau < 0.f || tau > 16.f) return ATTN_ERR_INVALID_ARG;
   settings();
@@ -361,6 +385,7 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* ls
   if (int st = make_map(&p.tm_q, q, BH, N, d_qk)) return st;
   if (int st = make_map(&p.tm_k, k, B * H_kv, N, d_qk)) return st;
   if (int st = make_map(&p.tm_v, v, B * H_kv, N, d_v)) return st;
+  if (int st = make_map(&p.tm_o, o, BH, N, d_v)) return st;
   if (int st = status_ptr(&p.status)) return st;
   p.o = o;
   p.lse = lse;
@@ -533,6 +558,7 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* sq
   if (int st = make_map(&p.tm_q, q8, BH, N, d, 128, 1)) return st;
   if (int st = make_map(&p.tm_k, k8, BH, N, d, 128, 1)) return st;
   if (int st = make_map(&p.tm_v, v8, BH, N, d, 128, 1)) return st;
+  if (int st = make_map(&p.tm_o, o, BH, N, d)) return st;
   if (int st = status_ptr(&p.status)) return st;
   p.o = o;
   p.lse = lse;
@@ -625,6 +651,11 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if (int st = make_map(&p.tm_do, dO, BH, N, d_v)) return st;
   p.h_q = H;
   p.kv_group = H / H_kv;
+  {
+    const int n_heads = B * H_kv;  // the units' heads (K/V heads)
+    p.det_group = (cfg.det_group > 0 && cfg.det_group < n_heads) ? cfg.det_group : n_heads;
+    p.det_desc = mask != nullptr ? 0 : cfg.det_desc;
+  }
   // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)
   p.pair_mode = (d_qk == 128 && cfg.bwd_pair && mask == nullptr && !gqa) ? 1 : 0;
   if (mask != nullptr) p.mask = *mask;
@@ -732,6 +763,7 @@ int attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float*
   if (int st = make_map(&p.tm_q, q, BH, N, d_qk)) return st;
   if (int st = make_map(&p.tm_k, k, BH, N, d_qk)) return st;
   if (int st = make_map(&p.tm_v, v, BH, N, d_v)) return st;
+  if (int st = make_map(&p.tm_o, o, BH, N, d_v)) return st;
   if (int st = status_ptr(&p.status)) return st;
   p.o = o;
   p.lse = lse;

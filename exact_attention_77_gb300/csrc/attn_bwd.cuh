@@ -126,6 +126,31 @@ __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Deterministic mode's order of the (head, key tile) work units: key-tile-
+// major inside groups of ``group`` heads (the heads of a group interleaved),
+// key tiles ascending, or from the last down with ``desc``.  Every dQ tile
+// takes its key-tile contributions in that same order (det_rank), so a unit
+// waits only on units of its own head that come earlier in the order: with
+// CTAs launched (or persistent CTAs taking units) in increasing order, the
+// waits always point backwards.  group = all heads keeps each head's key
+// tiles close in time (short ticket chains) but spreads the resident CTAs'
+// dQ additions over every head's accumulator; small groups do the opposite.
+__device__ __forceinline__ void det_unit(int u, int n_heads, int n, int group, int desc, int& j, int& bh) {
+  const int grp = u / (group * n);
+  const int h0 = grp * group;
+  const int g = min(group, n_heads - h0);  // heads in this (possibly last, smaller) group
+  const int rem = u - h0 * n;
+  const int jj = rem / g;
+  bh = h0 + (rem - jj * g);
+  j = desc ? n - 1 - jj : jj;
+}
+
+// Position of key tile j among the contributions to query tile i (the ticket
+// value at which its dQ addition may go ahead).
+__device__ __forceinline__ int det_rank(int i, int j, int n, bool causal, int desc) {
+  return desc ? (causal ? i : n - 1) - j : j;
+}
+
 // -------------------------------------------------------------- preprocess
 // One group of D/8 lanes per row, 16-byte loads.
 template <int D>
@@ -226,9 +251,8 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
   const int n = p.n_tiles;
   const int n_heads = GQA ? p.BH / p.kv_group : p.BH;  // K/V heads
   int j, bh;
-  if (DETERMINISTIC) {  // key-tile-major: a CTA waits only on CTAs launched before it
-    j = blockIdx.x / n_heads;
-    bh = blockIdx.x - j * n_heads;
+  if (DETERMINISTIC) {  // a CTA waits only on CTAs launched before it
+    det_unit(blockIdx.x, n_heads, n, MASK ? n_heads : p.det_group, MASK ? 0 : p.det_desc, j, bh);
   } else {  // head-major: resident CTAs share one or two heads' dQ accumulators in L2
     bh = blockIdx.x / n;
     j = blockIdx.x - bh * n;
@@ -619,6 +643,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       const int i = tile_i(qi);
       const int qh = head_q(qi);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
+      ok = named_bar_and(1, 128, ok);  // the four warps leave together (named barriers below)
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 9);
       tc_fence_after();
@@ -661,7 +686,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
           if (DETERMINISTIC && r == 0) {
             const uint64_t t0 = globaltimer_ns();
             // tile i takes its (visible) key tiles in ascending order
-            int rank = j;
+            int rank = det_rank(i, j, n, CAUSAL, p.det_desc);
             if (MASK) {
               rank = 0;
               for (int jj = 0; jj < j; ++jj) rank += mask_tile_visible(p.mask, i, jj) ? 1 : 0;

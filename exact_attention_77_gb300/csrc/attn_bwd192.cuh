@@ -175,8 +175,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
   const int n_heads = GQA ? p.BH / p.kv_group : p.BH;
   int j, bh;
   if (DETERMINISTIC) {
-    j = blockIdx.x / n_heads;
-    bh = blockIdx.x - j * n_heads;
+    det_unit(blockIdx.x, n_heads, n, p.det_group, p.det_desc, j, bh);
   } else {
     bh = blockIdx.x / n;
     j = blockIdx.x - bh * n;
@@ -544,6 +543,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       const int i = tile_i(qi);
       const int qh = head_q(qi);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kB192WhereDq));
+      ok = named_bar_and(1, 128, ok);  // the four warps leave together (named barriers below)
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 21);
       tc_fence_after();
@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
         if (tid == 0) {
           if (DETERMINISTIC && r == 0) {
             const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(ticket) != j) {  // key tiles add in ascending order
+            while (ld_acquire_gpu(ticket) != det_rank(i, j, n, CAUSAL, p.det_desc)) {  // the fixed order
               if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
                 if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
                 *ctl.abort = 1;

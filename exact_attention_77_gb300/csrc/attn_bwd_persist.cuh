@@ -64,8 +64,7 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
   auto unit_at = [&](int u) {
     BUnit w;
     if (DETERMINISTIC) {
-      w.j = u / n_heads;
-      w.bh = u - w.j * n_heads;
+      det_unit(u, n_heads, n, p.det_group, p.det_desc, w.j, w.bh);
     } else {
       w.bh = u / n;
       w.j = u - w.bh * n;
@@ -521,6 +520,7 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       const int i = tile_i(qi);
       const int qh = head_q(w, qi);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), tt & 1, ctl, kBWhereDq));
+      ok = named_bar_and(1, 128, ok);  // the four warps leave together (named barriers below)
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 9);
       tc_fence_after();
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
           if (DETERMINISTIC && r == 0) {
             const uint64_t t0 = globaltimer_ns();
             // tile i takes its (visible) key tiles in ascending order
-            int rank = j;
+            int rank = det_rank(i, j, n, CAUSAL, p.det_desc);
             if (MASK) {
               rank = 0;
               for (int jj = 0; jj < j; ++jj) rank += mask_tile_visible(p.mask, i, jj) ? 1 : 0;
@@ -614,9 +614,25 @@ cudaError_t launch_bwd_persist_main(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, &sms);
   if (e != cudaSuccess) return e;
   const int n_units = p.BH * p.n_tiles;
-  // one CTA per SM, all resident (the deterministic mode's waits only point
-  // to units taken earlier)
-  kernel<<<n_units < sms ? n_units : sms, L::kThreads, L::kSmemBytes, stream>>>(p);
+  const int grid = n_units < sms ? n_units : sms;  // one CTA per SM
+  if constexpr (DET) {
+    // Deterministic mode: a unit's dQ additions wait for lower-numbered units,
+    // which on later rounds belong to other CTAs (some with a higher index),
+    // so every CTA must be resident at once.  A cooperative launch guarantees
+    // that even while other kernels hold part of the GPU (or fails up front).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+  }
+  kernel<<<grid, L::kThreads, L::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

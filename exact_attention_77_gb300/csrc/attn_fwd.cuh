@@ -58,10 +58,13 @@ struct FwdLayout {
   static constexpr int kPVKeys = 32 / ES;             // keys per P V product
   static constexpr int kStageBytes = kKBytes > kVBytes ? kKBytes : kVBytes;
   static constexpr int kQRegion = NQT * kQBytes;
+  // Epilogue staging per query tile: one [128 rows x 64 columns] bf16 box of
+  // O in the 128-byte swizzled layout the TMA store reads.
+  static constexpr int kStgBytes = kTile * 64 * 2;
   // One query tile per CTA is sized so two CTAs share an SM (two softmax
   // warpgroups per SM either way); two tiles take the SM alone.
-  static constexpr int kBudget = NQT == 1 ? 110 * 1024 : 226 * 1024;
-  static constexpr int kStagesFit = (kBudget - kQRegion) / kStageBytes;
+  static constexpr int kBudget = NQT == 1 ? 112 * 1024 : 226 * 1024;
+  static constexpr int kStagesFit = (kBudget - kQRegion - NQT * kStgBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
   static_assert(kStages >= 2, "K/V ring needs two stages");
   static constexpr int kThreads = 128 + 128 * NQT;
@@ -74,7 +77,8 @@ struct FwdLayout {
   static constexpr int kSmRegs = NQT == 1 ? 208 : 208;
   static_assert(kCtlRegs * 128 + kSmRegs * 128 * NQT == kLaunchRegs * kThreads, "register split");
   static constexpr int kKVOff = kQRegion;
-  static constexpr int kBarOff = kKVOff + kStages * kStageBytes;
+  static constexpr int kStgOff = kKVOff + kStages * kStageBytes;
+  static constexpr int kBarOff = kStgOff + NQT * kStgBytes;
   static constexpr int kBarQFull = 0;
   static constexpr int kBarKVFull = 1;
   static constexpr int kBarKVEmpty = kBarKVFull + kStages;
@@ -606,8 +610,11 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       mbar_arrive(bar(L::kBarPFull + t));
       if (quad == 0 && lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 10 + 2 * t);
     }
-    if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), cbit ^ ((n - 1) & 1), ctl, kWhereSmFinal));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone + t), cbit ^ ((n - 1) & 1), ctl, kWhereSmFinal));
+    // the four warps of the warpgroup agree (the epilogue's named barriers
+    // need all of them, and after a timeout all of them leave together)
+    ok = named_bar_and(1 + t, 128, ok);
+    {
       if (ok) {
         tc_fence_after();
         const float inv_l = l > 0.f ? (FP8 ? p.sv[bh] : 1.f) / l : 0.f;
@@ -632,25 +639,42 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
           }
           if (live) p.lse_part[prow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         } else {
-          uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                                 ((size_t)bh * p.N + (live ? q_row : 0)) * DV);
+          float o[DV];
 #pragma unroll
-          for (int c0 = 0; c0 < DV; c0 += 32) {
-            float o[32];
-            tmem_ld32(tO + c0, o);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
-            if (live) {
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            }
-          }
+          for (int c0 = 0; c0 < DV; c0 += 32) tmem_ld32p(tO + c0, o + c0);
           // O_t has been read out: the next unit's products may overwrite it
           if (PERSIST) {
             tc_fence_before();
             mbar_arrive(bar(L::kBarOFree + t));
+          }
+          // O / l as bf16, one 64-column box at a time: each thread writes its
+          // row into the staging tile in the 128-byte swizzled layout (16-byte
+          // unit c of row r at unit c ^ (r % 8): a quarter warp covers all 32
+          // banks), then one thread hands the box to the copy engine, whose
+          // TMA store writes whole rows to global memory and leaves out the
+          // rows past N.  The staging tile is reused once the previous box's
+          // store has read it.
+          const int r_in = quad * 32 + lane;
+          const bool issuer = quad == 0 && lane == 0;
+          uint8_t* srow = smem + L::kStgOff + t * L::kStgBytes + r_in * 128;
+          const uint32_t stile = sbase + L::kStgOff + t * L::kStgBytes;
+#pragma unroll
+          for (int b = 0; b < DV / 64; ++b) {
+            if (issuer) bulk_wait_read<0>();
+            named_bar_sync(1 + t, 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const float* v = o + b * 64 + 8 * c;
+              *reinterpret_cast<uint4*>(srow + ((c ^ (r_in & 7)) * 16)) =
+                  make_uint4(pack_bf16(v[0] * inv_l, v[1] * inv_l), pack_bf16(v[2] * inv_l, v[3] * inv_l),
+                             pack_bf16(v[4] * inv_l, v[5] * inv_l), pack_bf16(v[6] * inv_l, v[7] * inv_l));
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + t, 128);
+            if (issuer) {
+              tma_store_3d(&p.tm_o, stile, b * 64, qt * kTile, bh);
+              bulk_commit();
+            }
           }
           if (live)
             p.lse[(size_t)bh * p.N + q_row] = l > 0.f ? (m - kPOff + __log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -659,6 +683,8 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     }
     cbit ^= (uint32_t)(n & 1);
     }  // units
+    if (quad == 0 && lane == 0) bulk_wait_all<0>();  // the epilogue's TMA stores are complete before exit
+    __syncwarp();
     if (p.rescale_counter != nullptr) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) rescales += __shfl_xor_sync(0xffffffffu, rescales, off);

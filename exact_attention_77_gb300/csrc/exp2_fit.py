@@ -8,8 +8,8 @@ pages print no coefficients, so they are fitted here: p(0) = 1 is fixed
 [0, 1] is minimised by Lawson's iteratively reweighted least squares, which
 converges to the minimax solution.
 
-Run ``python exp2_fit.py`` to print the constants pasted into sm103.cuh and
-exp2_probe.cu.
+Run ``python exp2_fit.py`` to print the constants pasted into sm103.cuh (the
+cubic the forward kernel uses) and probes.cu (degrees 4 and 5).
 """
 import numpy as np
 

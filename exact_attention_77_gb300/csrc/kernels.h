@@ -25,6 +25,7 @@ struct FwdParams {
   CUtensorMap tm_q;  // [BH, N, d_qk] bf16, box 64 x 128 x 1, 128-byte swizzle
   CUtensorMap tm_k;  // [BH, N, d_qk]
   CUtensorMap tm_v;  // [BH, N, d_v]
+  CUtensorMap tm_o;  // [BH, N, d_v] bf16 output, box 64 x 128 x 1 (the epilogue's TMA stores)
   void* o;           // bf16 [BH, N, d_v]
   float* lse;        // fp32 [BH, N]
   DeviceStatus* status;
@@ -93,6 +94,11 @@ struct BwdParams {
   int h_q;
   int kv_group;
   int persist;  // 1: persistent CTAs (one per SM) over the (head, key tile) units
+  // deterministic mode's unit order (det_unit in attn_bwd.cuh): key-tile-major
+  // inside groups of det_group heads (1 .. K/V heads); det_desc = 1 takes the
+  // key tiles from the last down (and each dQ tile adds them in that order)
+  int det_group;
+  int det_desc;
 };
 
 // Optional events recorded on the launch stream around each backward kernel:

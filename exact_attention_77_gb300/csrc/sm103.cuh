@@ -147,6 +147,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Shared -> global store of one box through a tensor map, tracked by the
+// issuing thread's bulk async-groups (bulk_commit / bulk_wait_*).  Parts of
+// the box outside the tensor are not written.  x * element size must be a
+// multiple of 16 bytes and no coordinate may be negative.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Brings one tile of a tensor map into L2 (no shared memory, no completion
 // signal); the same coordinates as tma_load_3d.
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
@@ -199,6 +210,21 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier over ``nthreads`` threads that also returns the AND of ``v``
+// over all of them (every participant sees the same answer).
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ----------------------------------------------------------------- tcgen05

@@ -335,6 +335,20 @@ int attn_set_rescale_counter(unsigned long long* counter);
 int attn_set_rescale_threshold(float tau);
 
 /*
+ * Exponential path of the bf16 forward ("FlashAttention-4: Algorithm and
+ * Kernel Pipelining Co-Design for Asymmetric Hardware Scaling", abstract and
+ * Table 2; "FlashAttention 3 and 4: When the Bottleneck Moves", section 3.2:
+ * a share of the exponentials emulated on the FMA pipe by a polynomial).
+ * enable = 1: later attn_fwd / attn_fwd_gqa calls evaluate 10 of every 32
+ * score columns as 2^floor(x) * p3(x - floor(x)) with the degree-3 minimax
+ * polynomial on FMAs and the other 22 on the hardware ex2 unit; enable = 0
+ * (the default; also the environment variable ATTN_EXP_POLY=0/1 at first use)
+ * uses the hardware unit for every column.  Results meet the same tolerances
+ * either way.  Returns ATTN_OK or ATTN_ERR_INVALID_ARG (enable not 0 or 1).
+ */
+int attn_set_exp_poly(int enable);
+
+/*
  * Backward on CTA pairs at d = 128 ("FlashAttention-4: Algorithm and Kernel
  * Pipelining Co-Design for Asymmetric Hardware Scaling", Table 3 and Figure
  * 3: the 2-CTA backward).  With enable = 1, later attn_bwd calls with
@@ -360,10 +374,35 @@ int attn_set_bwd_pair(int enable);
  * tolerances either way; deterministic mode is bit-identical run to run with
  * either kernel (the two may differ from each other in the last bits).
  * Applies to d_qk = d_v = 64 and 128 without grouped-query heads or masks;
- * the other backward calls always run one CTA per unit.
+ * the other backward calls always run one CTA per unit.  At d = 128 the
+ * CTA-pair setting (attn_set_bwd_pair(1)) takes precedence: with it on, the
+ * pair kernel runs whatever this mode says.  In deterministic mode the
+ * persistent kernel is launched cooperatively (all its CTAs resident at once,
+ * which its cross-CTA ordering of the dQ additions needs, even while other
+ * kernels share the GPU).
  * Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
  */
 int attn_set_bwd_persist(int mode);
+
+/*
+ * Order of the work in the deterministic backward ("FlashAttention-4:
+ * Algorithm and Kernel Pipelining Co-Design for Asymmetric Hardware
+ * Scaling", Figures 7 and 8: the schedule ablations of the deterministic
+ * backward -- head swizzle, shortest- or longest-first, reverse m-block
+ * order).  The (head, key tile) units run key-tile-major inside groups of
+ * ``head_group`` heads (0 = all heads in one group, the default; also
+ * ATTN_DET_GROUP at first use); ``descending`` = 1 (ATTN_DET_DESC) takes the
+ * key tiles from the last down -- shortest first under the causal mask --
+ * and every dQ tile then adds its key-tile contributions in that same
+ * descending order, 0 ascending (longest first under the causal mask).
+ * Query tiles are always visited from the last down.  Each setting is
+ * bit-reproducible on its own; different settings add in different orders
+ * and may differ from each other in the last bits.  Applies to later
+ * deterministic attn_bwd / attn_bwd_gqa / attn_bwd_noalloc calls except the
+ * CTA-pair kernel (masked calls always take the default).  Returns ATTN_OK
+ * or ATTN_ERR_INVALID_ARG (head_group < 0, descending not 0 or 1).
+ */
+int attn_set_det_schedule(int head_group, int descending);
 
 /*
  * Per-kernel timing for benchmarks.  Between attn_profile_start and

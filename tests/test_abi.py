@@ -127,6 +127,14 @@ def test_tuning_setters(lib):
     assert lib.get_lib().attn_set_bwd_persist(-2) == A.ATTN_ERR_INVALID_ARG
     for m in (1, 0, -1):
         assert lib.get_lib().attn_set_bwd_persist(m) == A.ATTN_OK
+    assert lib.get_lib().attn_set_exp_poly(2) == A.ATTN_ERR_INVALID_ARG
+    assert lib.get_lib().attn_set_exp_poly(-1) == A.ATTN_ERR_INVALID_ARG
+    assert lib.get_lib().attn_set_exp_poly(1) == A.ATTN_OK
+    assert lib.get_lib().attn_set_exp_poly(0) == A.ATTN_OK
+    assert lib.get_lib().attn_set_det_schedule(-1, 0) == A.ATTN_ERR_INVALID_ARG
+    assert lib.get_lib().attn_set_det_schedule(4, 2) == A.ATTN_ERR_INVALID_ARG
+    assert lib.get_lib().attn_set_det_schedule(4, 1) == A.ATTN_OK
+    assert lib.get_lib().attn_set_det_schedule(0, 0) == A.ATTN_OK
     assert lib.get_lib().attn_selftest_wait_timeout(0, None) == A.ATTN_ERR_INVALID_ARG
     assert lib.get_lib().attn_exp2_probe(None, None, 4, 0, None) == A.ATTN_ERR_INVALID_ARG
     assert lib.get_lib().attn_exp2_probe(0x1000, 0x1000, 4, 7, None) == A.ATTN_ERR_INVALID_ARG

@@ -79,3 +79,13 @@ def test_oracle_sample_draws_head_zero_of_the_workload(d, dv):
     f = {n: ora.bf16_to_f64(full[n])[0, 0] for n in ("q", "k", "v", "do")}
     assert np.array_equal(q, f["q"][:17]) and np.array_equal(k, f["k"])
     assert np.array_equal(v, f["v"]) and np.array_equal(do, f["do"][:17])
+
+
+def test_roofline_peak_is_burst_unless_power_capped():
+    peaks = {"bf16_tflops": 1943.4, "bf16_tflops_sustained": 1698.1}
+    p, note = bench.roofline_peak(peaks, {"reasons": []})
+    assert p == 1943.4 and "burst" in note
+    p, note = bench.roofline_peak(peaks, {"reasons": ["sw_power_cap"]})
+    assert p == 1698.1 and "power cap" in note
+    p, _ = bench.roofline_peak({}, {"reasons": None})
+    assert p == bench.FALLBACK_PEAKS["bf16_tflops"]
