@@ -607,11 +607,11 @@ def run_detsched_case(args, A, torch, dev, out):
         return statistics.median(ts)
 
     rows = {"atomic": main_ms(0)}
-    groups = [g for g in (1, 2, 4, 8) if g < B * H] + [0]
+    groups = [g for g in (1, 2, 4, 8) if g < B * H] + [B * H]  # the last: one group of all heads
     for desc in (0, 1):
         for g in groups:
             A.attn_set_det_schedule(g, desc)
-            rows[f"group={g or 'all'} {'desc' if desc else 'asc'}"] = main_ms(1)
+            rows[f"group={g if g < B * H else 'all'} {'desc' if desc else 'asc'}"] = main_ms(1)
     A.attn_set_det_schedule(0, 0)
     out.update({"config": {"B": B, "H": H, "N": N, "d": d, "causal": bool(args.causal)},
                 "backward_main_ms": rows,

@@ -86,7 +86,12 @@ struct BwdLayout {
   static constexpr int kBarDQFull = kBarDSFull + 2;
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarAccDone = kBarDQFree + 1;
-  static constexpr int kNumBars = kBarAccDone + 1;
+  // deterministic mode: + w: a staging round of a tile for reducer warp w
+  // (tiles alternate between two reducers) is in shared memory (4 dQ-warp
+  // arrivals); the staging tile has been read by the copy engine (1 arrival)
+  static constexpr int kBarStgFull = kBarAccDone + 1;
+  static constexpr int kBarStgFree = kBarStgFull + 2;
+  static constexpr int kNumBars = kBarStgFree + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -287,6 +292,7 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       if ((b >= L::kBarPReady && b < L::kBarPReady + 2) || (b >= L::kBarDSFull && b < L::kBarDSFull + 2))
         cnt = 256;  // both compute warpgroups
       if (b == L::kBarDQFree) cnt = 128;  // the dQ warpgroup
+      if (b == L::kBarStgFull || b == L::kBarStgFull + 1) cnt = 4;  // the dQ warpgroup's warps
       mbar_init(bar(b), cnt);
     }
     *abort_flag = 0;
@@ -441,6 +447,63 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       }
       tc_commit(bar(L::kBarAccDone));
       mbar_wait_drain(bar(L::kBarAccDone), 0, p.timeout_ns);
+    }
+    __syncwarp();
+   } else if (DETERMINISTIC) {
+    // ==================== dQ reducers (deterministic mode) ====================
+    // Warps 2 and 3 take the query tiles in turn.  For each of its tiles a
+    // reducer waits for the staging rounds the dQ warpgroup writes, waits for
+    // the tile's ticket, hands each round to the copy engine as a bulk FP32
+    // reduce-add and frees the staging tile once it has been read; then it
+    // waits until its additions are complete and passes the ticket on.  That
+    // wait overlaps the other reducer's next tile, so neither the dQ
+    // warpgroup nor the products behind it wait for the completion of the
+    // additions.
+    if (lane == 0) {
+      const int w = warp - 2;
+      uint32_t seen = 0;  // completed phases of this reducer's staging barrier
+      bool ok = true;
+      for (int it = 0, qi = i_first; ok && it < n_it; ++it, qi = i_next(qi)) {
+        if ((it & 1) != w) continue;
+        const int i = tile_i(qi);
+        const int qh = head_q(qi);
+        float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(D * kBTile);
+        int* ticket = p.tickets + (size_t)qh * p.n_tiles + i;
+        constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
+        for (int r = 0; ok && r < L::kStgRounds; ++r) {
+          if (!(ok = mbar_wait(bar(L::kBarStgFull + w), seen & 1, ctl, kBWhereDq + 2))) break;
+          ++seen;
+          if (r == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            // tile i takes its (visible) key tiles in the schedule's order
+            int rank = det_rank(i, j, n, CAUSAL, p.det_desc);
+            if (MASK) {
+              rank = 0;
+              for (int jj = 0; jj < j; ++jj) rank += mask_tile_visible(p.mask, i, jj) ? 1 : 0;
+            }
+            while (ld_acquire_gpu(ticket) != rank) {
+              if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
+                if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
+                *ctl.abort = 1;
+                break;
+              }
+            }
+            fence_proxy_async_global();
+            if (*ctl.abort) ok = false;
+          }
+          if (!ok) break;
+          bulk_reduce_add_f32(gdst + (size_t)r * kGroupsPerRound * kBTile * 4,
+                              sbase + L::kStgOff, L::kStgBytes);
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(bar(L::kBarStgFree));  // the staging tile may be overwritten
+        }
+        if (!ok) break;
+        bulk_wait_all<0>();  // the additions are performed before the next key tile's
+        fence_proxy_async_global();
+        red_release_gpu_add(ticket, 1);
+      }
+      bulk_wait_all<0>();  // nothing in flight when the CTA exits
     }
     __syncwarp();
    }
@@ -643,7 +706,8 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       const int i = tile_i(qi);
       const int qh = head_q(qi);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kBWhereDq));
-      ok = named_bar_and(1, 128, ok);  // the four warps leave together (named barriers below)
+      // the four warps leave together (the atomic mode's named barriers below)
+      if (!DETERMINISTIC) ok = named_bar_and(1, 128, ok);
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 9);
       tc_fence_after();
@@ -664,9 +728,33 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       // engine as a bulk FP32 reduce-add.  The staging tile is reused once
       // the previous tile's bulk read of it has finished.
       float* stg = reinterpret_cast<float*>(smem + L::kStgOff);
+      constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
+      if constexpr (DETERMINISTIC) {
+        // the reducer warps (above) issue the additions in ticket order; here
+        // each round is staged once the previous round has been read
+#pragma unroll
+        for (int r = 0; r < L::kStgRounds && ok; ++r) {
+          const int g_round = it * L::kStgRounds + r;  // staging rounds so far
+          if (g_round > 0)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(L::kBarStgFree), (uint32_t)(g_round - 1) & 1, ctl, kBWhereDq + 1));
+          if (!ok) break;
+#pragma unroll
+          for (int g = 0; g < kGroupsPerRound; ++g) {
+            const int gg = r * kGroupsPerRound + g;
+            *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+                make_float4(dq[4 * gg], dq[4 * gg + 1], dq[4 * gg + 2], dq[4 * gg + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::kBarStgFull + (it & 1)));
+        }
+        if (!ok) break;
+        if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 11);
+        continue;
+      }
       float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(D * kBTile);
       int* ticket = DETERMINISTIC ? p.tickets + (size_t)qh * p.n_tiles + i : nullptr;
-      constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
 #pragma unroll
       for (int r = 0; r < L::kStgRounds; ++r) {
         if (it > 0 || r > 0) {  // the previous round's bulk read of the staging tile

@@ -19,7 +19,7 @@ namespace attn {
 template <int D>
 struct BwdPLayout : BwdLayout<D> {
   using B = BwdLayout<D>;
-  static constexpr int kBarKVEmpty = B::kBarAccDone + 1;
+  static constexpr int kBarKVEmpty = B::kNumBars;
   static constexpr int kBarAccFree = kBarKVEmpty + 1;
   static constexpr int kBarMmaDrain = kBarAccFree + 1;
   static constexpr int kNumBars = kBarMmaDrain + 1;
@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
         cnt = 256;  // both compute warpgroups
       if (b == L::kBarDQFree) cnt = 128;  // the dQ warpgroup
       if (b == L::kBarAccFree) cnt = 256;  // both compute warpgroups
+      if (b == L::kBarStgFull || b == L::kBarStgFull + 1) cnt = 4;  // the dQ warpgroup's warps
       mbar_init(bar(b), cnt);
     }
     *abort_flag = 0;
@@ -295,6 +296,63 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       tc_commit(bar(L::kBarMmaDrain));
       mbar_wait_drain(bar(L::kBarMmaDrain), 0, p.timeout_ns);
 
+    }
+    __syncwarp();
+   } else if (DETERMINISTIC) {
+    // ==================== dQ reducers (deterministic mode) ====================
+    // As in bwd_kernel: warps 2 and 3 take the CTA's tiles in turn (counted
+    // over all of its units), issue each tile's staged rounds in ticket order,
+    // free the staging tile after each read and pass the ticket on once the
+    // additions are complete, overlapping that wait with the other reducer.
+    if (lane == 0) {
+      const int wr = warp - 2;
+      uint32_t seen = 0;  // completed phases of this reducer's staging barrier
+      bool ok = true;
+      int t = 0;  // tiles of earlier units
+      for (int rd = 0; ok && rd < n_rounds; ++rd) {
+        const int u = unit_of_round(rd);
+        if (PERSIST && u >= n_units) continue;
+        const BUnit w = unit_at(u);
+        const int j = w.j;
+        for (int it = 0, qi = w.i_first; ok && it < w.n_it; ++it, qi = i_next(w, qi)) {
+          const int tt = t + it;
+          if ((tt & 1) != wr) continue;
+          const int i = tile_i(qi);
+          const int qh = head_q(w, qi);
+          float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(D * kBTile);
+          int* ticket = p.tickets + (size_t)qh * p.n_tiles + i;
+          constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
+          for (int r = 0; ok && r < L::kStgRounds; ++r) {
+            if (!(ok = mbar_wait(bar(L::kBarStgFull + wr), seen & 1, ctl, kBWhereDq + 2))) break;
+            ++seen;
+            if (r == 0) {
+              const uint64_t t0 = globaltimer_ns();
+              const int rank = det_rank(i, j, n, CAUSAL, p.det_desc);
+              while (ld_acquire_gpu(ticket) != rank) {
+                if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
+                  if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
+                  *ctl.abort = 1;
+                  break;
+                }
+              }
+              fence_proxy_async_global();
+              if (*ctl.abort) ok = false;
+            }
+            if (!ok) break;
+            bulk_reduce_add_f32(gdst + (size_t)r * kGroupsPerRound * kBTile * 4, sbase + L::kStgOff,
+                                L::kStgBytes);
+            bulk_commit();
+            bulk_wait_read<0>();
+            mbar_arrive(bar(L::kBarStgFree));  // the staging tile may be overwritten
+          }
+          if (!ok) break;
+          bulk_wait_all<0>();  // the additions are performed before the next key tile's
+          fence_proxy_async_global();
+          red_release_gpu_add(ticket, 1);
+        }
+        t += w.n_it;
+      }
+      bulk_wait_all<0>();  // nothing in flight when the CTA exits
     }
     __syncwarp();
    }
@@ -520,7 +578,8 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       const int i = tile_i(qi);
       const int qh = head_q(w, qi);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), tt & 1, ctl, kBWhereDq));
-      ok = named_bar_and(1, 128, ok);  // the four warps leave together (named barriers below)
+      // the four warps leave together (the atomic mode's named barriers below)
+      if (!DETERMINISTIC) ok = named_bar_and(1, 128, ok);
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 9);
       tc_fence_after();
@@ -541,9 +600,32 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       // engine as a bulk FP32 reduce-add.  The staging tile is reused once
       // the previous tile's bulk read of it has finished.
       float* stg = reinterpret_cast<float*>(smem + L::kStgOff);
+      constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
+      if constexpr (DETERMINISTIC) {
+        // the reducer warps issue the additions in ticket order; each round is
+        // staged once the previous round has been read
+#pragma unroll
+        for (int r = 0; r < L::kStgRounds && ok; ++r) {
+          const int g_round = tt * L::kStgRounds + r;  // staging rounds so far
+          if (g_round > 0)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(L::kBarStgFree), (uint32_t)(g_round - 1) & 1, ctl, kBWhereDq + 1));
+          if (!ok) break;
+#pragma unroll
+          for (int g = 0; g < kGroupsPerRound; ++g) {
+            const int gg = r * kGroupsPerRound + g;
+            *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+                make_float4(dq[4 * gg], dq[4 * gg + 1], dq[4 * gg + 2], dq[4 * gg + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::kBarStgFull + (tt & 1)));
+        }
+        if (!ok) break;
+        continue;
+      }
       float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(D * kBTile);
       int* ticket = DETERMINISTIC ? p.tickets + (size_t)qh * p.n_tiles + i : nullptr;
-      constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
 #pragma unroll
       for (int r = 0; r < L::kStgRounds; ++r) {
         if (tt > 0 || r > 0) {  // the previous round's bulk read of the staging tile

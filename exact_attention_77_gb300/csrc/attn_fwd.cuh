@@ -654,14 +654,21 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
           // TMA store writes whole rows to global memory and leaves out the
           // rows past N.  The staging tile is reused once the previous box's
           // store has read it.
+          // Without persistent CTAs the tile's Q region is free by now (its
+          // last S product has completed) and, when it holds all of O's
+          // boxes, takes them side by side: no box waits for another's store.
+          constexpr bool kInQ = !PERSIST && L::kQBytes >= DV * kTile * 2;
+          constexpr uint32_t kBoxStride = kInQ ? kTile * 128 : 0;
+          const uint32_t s_off = kInQ ? (uint32_t)(t * L::kQBytes) : (uint32_t)(L::kStgOff + t * L::kStgBytes);
           const int r_in = quad * 32 + lane;
           const bool issuer = quad == 0 && lane == 0;
-          uint8_t* srow = smem + L::kStgOff + t * L::kStgBytes + r_in * 128;
-          const uint32_t stile = sbase + L::kStgOff + t * L::kStgBytes;
 #pragma unroll
           for (int b = 0; b < DV / 64; ++b) {
-            if (issuer) bulk_wait_read<0>();
-            named_bar_sync(1 + t, 128);
+            uint8_t* srow = smem + s_off + b * kBoxStride + r_in * 128;
+            if (!kInQ) {  // the previous box's store has read the staging tile
+              if (issuer) bulk_wait_read<0>();
+              named_bar_sync(1 + t, 128);
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const float* v = o + b * 64 + 8 * c;
@@ -669,11 +676,14 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
                   make_uint4(pack_bf16(v[0] * inv_l, v[1] * inv_l), pack_bf16(v[2] * inv_l, v[3] * inv_l),
                              pack_bf16(v[4] * inv_l, v[5] * inv_l), pack_bf16(v[6] * inv_l, v[7] * inv_l));
             }
-            fence_proxy_async_smem();
-            named_bar_sync(1 + t, 128);
-            if (issuer) {
-              tma_store_3d(&p.tm_o, stile, b * 64, qt * kTile, bh);
-              bulk_commit();
+            if (!kInQ || b == DV / 64 - 1) {
+              fence_proxy_async_smem();
+              named_bar_sync(1 + t, 128);
+              if (issuer) {
+                for (int bb = kInQ ? 0 : b; bb <= b; ++bb)
+                  tma_store_3d(&p.tm_o, sbase + s_off + bb * kBoxStride, bb * 64, qt * kTile, bh);
+                bulk_commit();
+              }
             }
           }
           if (live)
@@ -683,7 +693,9 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     }
     cbit ^= (uint32_t)(n & 1);
     }  // units
-    if (quad == 0 && lane == 0) bulk_wait_all<0>();  // the epilogue's TMA stores are complete before exit
+    // the epilogue's TMA stores have read the staging tile before the CTA
+    // exits (their global writes complete on their own)
+    if (quad == 0 && lane == 0) bulk_wait_read<0>();
     __syncwarp();
     if (p.rescale_counter != nullptr) {
 #pragma unroll
