@@ -574,12 +574,6 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
             }
             fence_proxy_async_global();
           }
-          // the next query tile's Q load was issued before this tile's dQ
-          // product (when dK released the single Q stage); the copy engine
-          // takes it first, ahead of this tile's 96 KiB of reduce-adds, so
-          // the next S^T does not wait behind them (observation only)
-          if (r == 0 && it + 1 < n_it && !*ctl.abort)
-            mbar_wait(bar(L::kBarQFull), (uint32_t)(it + 1) & 1, ctl, kB192WhereDq + 1);
           if (!*ctl.abort) {
             bulk_reduce_add_f32(gdst + (size_t)r * 16 * kBTile * 4, smem_u32(stg), L::kStgBytes);
             bulk_commit();
