@@ -65,7 +65,12 @@ struct Bwd192Layout {
   static constexpr int kBarDQFreeX = 13;   // 128 arrivals: dQ columns over X read
   static constexpr int kBarDQFreePK = 14;  // 128 arrivals: dQ columns over PK read
   static constexpr int kBarAccDone = 15;
-  static constexpr int kNumBars = 16;
+  // deterministic mode (as in bwd_kernel): + w: a staging round of a tile of
+  // reducer warp w is staged (4 dQ-warp arrivals); the staging tile has been
+  // read by the copy engine (1 arrival)
+  static constexpr int kBarStgFull = 16;
+  static constexpr int kBarStgFree = 18;
+  static constexpr int kNumBars = 19;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -203,6 +208,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       uint32_t cnt = 1;
       if (b == L::kBarPReady || b == L::kBarPReady + 1 || b == L::kBarDSFull || b == L::kBarDSFull + 1) cnt = 256;
       if (b == L::kBarDQFreeX || b == L::kBarDQFreePK) cnt = 128;
+      if (b == L::kBarStgFull || b == L::kBarStgFull + 1) cnt = 4;  // the dQ warpgroup's warps
       mbar_init(bar(b), cnt);
     }
     *abort_flag = 0;
@@ -355,6 +361,53 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
         }
         tc_commit(bar(L::kBarAccDone));
         mbar_wait_drain(bar(L::kBarAccDone), 0, p.timeout_ns);
+      }
+      __syncwarp();
+    } else if (DETERMINISTIC) {
+      // ================= dQ reducers (deterministic mode) ==================
+      // Warps 2 and 3 take the query tiles in turn: for each of the tile's
+      // three staged rounds the reducer waits for it, (first round) waits for
+      // the tile's ticket, hands it to the copy engine as a bulk FP32
+      // reduce-add and frees the staging tile once read; after the last round
+      // it waits for the additions to complete and passes the ticket on,
+      // while the other reducer already serves the next tile.
+      if (lane == 0) {
+        const int w = warp - 2;
+        uint32_t seen = 0;  // completed phases of this reducer's staging barrier
+        bool ok = true;
+        for (int it = 0, qi = i_first; ok && it < n_it; ++it, qi = i_next(qi)) {
+          if ((it & 1) != w) continue;
+          const int i = tile_i(qi);
+          const int qh = head_q(qi);
+          float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(DQK * kBTile);
+          int* ticket = p.tickets + (size_t)qh * p.n_tiles + i;
+          for (int r = 0; ok && r < L::kStgRounds; ++r) {
+            if (!(ok = mbar_wait(bar(L::kBarStgFull + w), seen & 1, ctl, kB192WhereDq + 2))) break;
+            ++seen;
+            if (r == 0) {
+              const uint64_t t0 = globaltimer_ns();
+              while (ld_acquire_gpu(ticket) != det_rank(i, j, n, CAUSAL, p.det_desc)) {  // the fixed order
+                if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
+                  if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
+                  *ctl.abort = 1;
+                  break;
+                }
+              }
+              fence_proxy_async_global();
+              if (*ctl.abort) ok = false;
+            }
+            if (!ok) break;
+            bulk_reduce_add_f32(gdst + (size_t)r * 16 * kBTile * 4, sbase + L::kStgOff, L::kStgBytes);
+            bulk_commit();
+            bulk_wait_read<0>();
+            mbar_arrive(bar(L::kBarStgFree));  // the staging tile may be overwritten
+          }
+          if (!ok) break;
+          bulk_wait_all<0>();  // the additions are performed before the next key tile's
+          fence_proxy_async_global();
+          red_release_gpu_add(ticket, 1);
+        }
+        bulk_wait_all<0>();  // nothing in flight when the CTA exits
       }
       __syncwarp();
     }
@@ -543,7 +596,8 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       const int i = tile_i(qi);
       const int qh = head_q(qi);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, ctl, kB192WhereDq));
-      ok = named_bar_and(1, 128, ok);  // the four warps leave together (named barriers below)
+      // the four warps leave together (the atomic mode's named barriers below)
+      if (!DETERMINISTIC) ok = named_bar_and(1, 128, ok);
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 21);
       tc_fence_after();
@@ -551,6 +605,23 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       int* ticket = DETERMINISTIC ? p.tickets + (size_t)qh * p.n_tiles + i : nullptr;
       // stage 16 column groups (64 columns) from v and hand them to the copy engine
       auto round = [&](int r, const float* v) {
+        if constexpr (DETERMINISTIC) {
+          // the reducer warps (above) issue the additions in ticket order;
+          // the round is staged once the previous round has been read
+          const int g_round = it * L::kStgRounds + r;
+          if (ok && g_round > 0)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(L::kBarStgFree), (uint32_t)(g_round - 1) & 1, ctl, kB192WhereDq + 1));
+          if (!ok) return;
+#pragma unroll
+          for (int g = 0; g < 16; ++g)
+            *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+                make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::kBarStgFull + (it & 1)));
+          return;
+        }
         if (it > 0 || r > 0) {  // the previous round's bulk read of the staging tile
           if (tid == 0) bulk_wait_read<0>();
           __syncwarp();
@@ -595,11 +666,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       round(1, b);
       round(2, a);
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 24);
-      if (DETERMINISTIC && tid == 0) {
-        bulk_wait_all<0>();
-        fence_proxy_async_global();
-        if (!*ctl.abort) red_release_gpu_add(ticket, 1);
-      }
+      if (DETERMINISTIC && !ok) break;
       __syncwarp();
     }
     if (tid == 0) bulk_wait_all<0>();
