@@ -16,7 +16,7 @@ fraction of the measured dense BF16 peak.
 --impl reference times the FP64 CPU oracle on the host cores (a bounded sample
 of the same workload per step).
 
-  python bench.py --case fp8|splitkv|masked|exp2|detsched [--B --H --N ...]
+  python bench.py --case fp8|splitkv|masked|exp2|detsched|sweep [--B --H --N ...]
 
 times one of the library's other paths instead (one GPU; a JSON line with its
 own fields; no contract line): the FP8 quantiser + FP8 forward, the split-KV
@@ -24,7 +24,8 @@ decode forward (--Nq queries against --Nk keys, the heuristic's ranges), or
 the masked forward + backward (--window-left / --window-right, --block-density
 for a seeded random block map), or the exponential paths' accuracy (the
 experiment of Table 2 of the FlashAttention-4 paper) and throughput per SM
-per clock, or the deterministic backward under each unit order (detsched).
+per clock, the deterministic backward under each unit order (detsched), or
+every configuration of the workload list, forward and backward (sweep).
 Under torchrun every rank runs the same
 workload on its own GPU (independent replicas: no data exchange), timing is
 bracketed by barriers and the slowest rank's time is used.
@@ -205,12 +206,13 @@ def strip_c_comments(text: str) -> str:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources' code (comments excluded): the committed DRAM
-    counters stay valid while it is unchanged."""
+    """Hash of the kernel sources' code (comments excluded; the C-ABI host file
+    left out): the committed DRAM counters stay valid while it is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_77_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        # the kernels and their headers (the C-ABI host code does not change a kernel's traffic)
+        if name.endswith((".cu", ".cuh", ".h")) and name != "attn_api.cu":
             with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 h.update(name.encode() + strip_c_comments(f.read()).encode())
     return h.hexdigest()[:16]
@@ -619,6 +621,66 @@ def run_detsched_case(args, A, torch, dev, out):
                 "note": "deterministic backward main kernel per unit order; group = heads per key-tile-major group"})
 
 
+def run_sweep_case(args, A, torch, dev, out):
+    """Every configuration of the workload list: forward TFLOP/s (configs 1-4)
+    and backward TFLOP/s in both dQ modes (configs 1, 5 and the d_qk = 192
+    backward), each the median of --steps calls after --warmup, the L2
+    flushed before each call; kernel times from the library's per-kernel
+    events (backward: the main kernel, and the whole call with its
+    preprocess and dQ conversion)."""
+    import synth
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def med(fn, key):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i & 0xFF)
+            A.attn_profile_start()
+            fn()
+            pr = A.attn_profile_stop()
+            if i >= args.warmup:
+                ts.append(pr[key] if isinstance(key, str) else sum(pr[k] for k in key))
+        return statistics.median(ts)
+
+    rows = []
+
+    def point(name, B, H, N, dqk, dvh, causal, bwd):
+        t = synth.attention_inputs_torch(synth.AttentionShape(B, H, N, dqk, dvh), seed=0, with_do=bwd, device=dev)
+        o = torch.empty((B, H, N, dvh), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        sc = 1.0 / math.sqrt(dqk)
+        f = 2.0 * B * H * N * N * (dqk + dvh) / (2 if causal else 1)
+        fwd = lambda: A.attn_fwd(t["q"], t["k"], t["v"], o, lse, B, H, N, dqk, dvh, causal, sc)
+        row = {"config": name, "B": B, "H": H, "N": N, "d_qk": dqk, "d_v": dvh, "causal": bool(causal),
+               "forward_tflops": f / med(fwd, "ms_fwd") / 1e9}
+        if bwd:
+            fwd()
+            dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+            for det in (0, 1):
+                nb = A.attn_bwd_workspace_bytes(B, H, N, dqk, dvh, det)
+                ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+                bw = lambda: A.attn_bwd(t["q"], t["k"], t["v"], o, t["do"], lse, dq, dk, dv, B, H, N, dqk, dvh,
+                                        causal, sc, det, ws, nb)
+                tag = "deterministic" if det else "atomic"
+                row[f"backward_main_tflops_{tag}"] = 2.5 * f / med(bw, "ms_bwd_main") / 1e9
+                row[f"backward_call_tflops_{tag}"] = 2.5 * f / med(
+                    bw, ("ms_bwd_pre", "ms_bwd_main", "ms_bwd_convert")) / 1e9
+        rows.append(row)
+        torch.cuda.synchronize(dev)
+
+    point("1 (PR1)", 1, 2, 256, 64, 64, 0, True)
+    point("2", 2, 16, 2048, 128, 128, 0, False)
+    for N in (1024, 2048, 4096, 8192, 16384):
+        for c in (0, 1):
+            point("3/5", 16384 // N, 16, N, 128, 128, c, True)
+    for N in (1024, 2048, 4096, 8192, 16384):
+        point("4", 16384 // N, 16, N, 192, 128, 1, True)
+        point("4 (non-causal backward)", 16384 // N, 16, N, 192, 128, 0, True)
+    out.update({"config": {"sweep": "BASELINE configurations", "l2": "256 MiB flushed before each call"},
+                "rows": rows})
+
+
 def run_case(args):
     """Time the FP8, split-KV or masked path (CUDA events, L2 flushed before
     each timed call, median of --steps after --warmup)."""
@@ -651,8 +713,9 @@ def run_case(args):
         return statistics.median(ts)
 
     out = {"case": args.case, "steps": args.steps, "warmup": args.warmup, "data": "synthetic (seeded N(0,1) bf16)"}
-    if args.case in ("exp2", "detsched"):
-        (run_exp2_case if args.case == "exp2" else run_detsched_case)(args, A, torch, dev, out)
+    if args.case in ("exp2", "detsched", "sweep"):
+        {"exp2": run_exp2_case, "detsched": run_detsched_case, "sweep": run_sweep_case}[args.case](args, A, torch, dev,
+                                                                                              out)
         print(json.dumps(out), flush=True)
         return
     if args.case == "fp8":
@@ -747,7 +810,7 @@ def main(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="head groups pipelined through host copies and compute in the e2e leg")
     ap.add_argument("--e2e-streams", type=int, default=3, help="compute streams the e2e leg deals its groups to")
-    ap.add_argument("--case", choices=("step", "fp8", "splitkv", "masked", "exp2", "detsched"), default="step",
+    ap.add_argument("--case", choices=("step", "fp8", "splitkv", "masked", "exp2", "detsched", "sweep"), default="step",
                     help="step: the benchmark contract; others time the library's other paths")
     ap.add_argument("--Nq", type=int, default=1)
     ap.add_argument("--Nk", type=int, default=16384)

@@ -653,10 +653,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   p.kv_group = H / H_kv;
   {
     const int n_heads = B * H_kv;  // the units' heads (K/V heads)
-    // measured on GB300 (H = 16, d = 128): 8-head groups are 2-3 % faster
-    // than one all-head group without a mask; under the causal mask one
-    // group over all heads, longest key tiles first, is the fastest order
-    const int g = cfg.det_group > 0 ? cfg.det_group : (causal ? n_heads : 8);
+    // measured on GB300 (H = 16, d = 128): 8-head groups are 4-5 % faster
+    // than one all-head group without a mask on the one-unit kernel (N >=
+    // 4096); on the persistent kernel (N <= 2048) and under the causal mask
+    // one group over all heads, longest key tiles first, is the fastest
+    const bool persistent_det = N <= 2048;  // the deterministic backward's kernel choice below
+    const int g = cfg.det_group > 0 ? cfg.det_group : ((causal || persistent_det) ? n_heads : 8);
     p.det_group = g < n_heads ? g : n_heads;
     p.det_desc = mask != nullptr ? 0 : cfg.det_desc;
   }

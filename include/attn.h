@@ -391,8 +391,8 @@ int attn_set_bwd_persist(int mode);
  * backward -- head swizzle, shortest- or longest-first, reverse m-block
  * order).  The (head, key tile) units run key-tile-major inside groups of
  * ``head_group`` heads (0, the default, picks the fastest order measured on
- * GB300: groups of 8 heads without a causal mask, one group of all heads
- * with it; also ATTN_DET_GROUP at first use); ``descending`` = 1
+ * GB300: groups of 8 heads without a causal mask for N > 2048, one group of
+ * all heads otherwise; also ATTN_DET_GROUP at first use); ``descending`` = 1
  * (ATTN_DET_DESC) takes the
  * key tiles from the last down -- shortest first under the causal mask --
  * and every dQ tile then adds its key-tile contributions in that same
