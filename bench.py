@@ -610,15 +610,23 @@ def run_detsched_case(args, A, torch, dev, out):
 
     rows = {"atomic": main_ms(0)}
     groups = [g for g in (1, 2, 4, 8) if g < B * H] + [B * H]  # the last: one group of all heads
-    for desc in (0, 1):
-        for g in groups:
-            A.attn_set_det_schedule(g, desc)
-            rows[f"group={g if g < B * H else 'all'} {'desc' if desc else 'asc'}"] = main_ms(1)
+    # both main kernels: one CTA per unit, and persistent CTAs (all resident;
+    # without the causal mask they take the rotated walk)
+    for persist in (0, 1):
+        A.attn_set_bwd_persist(persist)
+        kind = "persistent" if persist else "one-unit"
+        rows[f"atomic {kind}"] = main_ms(0)
+        for desc in (0, 1):
+            for g in groups:
+                A.attn_set_det_schedule(g, desc)
+                rows[f"{kind} group={g if g < B * H else 'all'} {'desc' if desc else 'asc'}"] = main_ms(1)
     A.attn_set_det_schedule(0, 0)
+    A.attn_set_bwd_persist(-1)
     out.update({"config": {"B": B, "H": H, "N": N, "d": d, "causal": bool(args.causal)},
                 "backward_main_ms": rows,
                 "backward_main_tflops": {k: fl / v / 1e9 for k, v in rows.items()},
-                "note": "deterministic backward main kernel per unit order; group = heads per key-tile-major group"})
+                "note": ("deterministic backward main kernel per unit order and main kernel; group = heads per "
+                         "key-tile-major group; 'atomic' = the library's default kernel choice")})
 
 
 def run_sweep_case(args, A, torch, dev, out):

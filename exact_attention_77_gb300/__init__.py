@@ -42,6 +42,7 @@ _SIGS = {
     "attn_set_bwd_persist": (_I, [_I]),
     "attn_set_exp_poly": (_I, [_I]),
     "attn_set_det_schedule": (_I, [_I, _I]),
+    "attn_bwd_det_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t, _P]),
@@ -300,6 +301,24 @@ def attn_set_exp_poly(enable: int):
 
 def attn_set_det_schedule(head_group: int, descending: int):
     _check(get_lib().attn_set_det_schedule(int(head_group), int(descending)))
+
+
+def attn_bwd_det_plan(n_heads: int, n_tiles: int, n_ctas: int, head_group: int, descending: int = 0,
+                      causal: int = 0, rotated: int = 0) -> dict:
+    """The deterministic backward's plan as the kernels compute it (host only):
+    per unit u its head, key tile and first query tile, and rank[u, i], the
+    ticket value at which its dQ addition to query tile i goes ahead (-1: not
+    visited).  Returns numpy int32 arrays."""
+    import numpy as np
+    n_units = int(n_heads) * int(n_tiles)
+    head = np.zeros(n_units, np.int32)
+    key = np.zeros(n_units, np.int32)
+    first = np.zeros(n_units, np.int32)
+    rank = np.zeros((n_units, int(n_tiles)), np.int32)
+    _check(get_lib().attn_bwd_det_plan(int(n_heads), int(n_tiles), int(n_ctas), int(head_group), int(descending),
+                                       int(causal), int(rotated), head.ctypes.data, key.ctypes.data,
+                                       first.ctypes.data, rank.ctypes.data))
+    return {"head": head, "key_tile": key, "first_tile": first, "rank": rank}
 
 
 def attn_selftest_wait_timeout(timeout_us: int, stream=None):

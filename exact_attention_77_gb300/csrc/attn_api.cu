@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "attn.h"
+#include "det_order.h"
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -350,6 +351,32 @@ int attn_set_det_schedule(int head_group, int descending) {
   return ATTN_OK;
 }
 
+int attn_bwd_det_plan(int n_heads, int n_tiles, int n_ctas, int head_group, int descending, int causal, int rotated,
+                      int* unit_head, int* unit_key_tile, int* unit_first_tile, int* rank) {
+  if (n_heads < 1 || n_tiles < 1 || n_ctas < 1 || head_group < 1 || (descending != 0 && descending != 1) ||
+      (causal != 0 && causal != 1) || (rotated != 0 && rotated != 1) || (rotated && causal) ||
+      (long long)n_heads * n_tiles * n_tiles > (1ll << 28) || unit_head == nullptr || unit_key_tile == nullptr ||
+      unit_first_tile == nullptr || rank == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  const int n = n_tiles;
+  const int group = head_group < n_heads ? head_group : n_heads;
+  for (int u = 0; u < n_heads * n; ++u) {
+    const attn::DetUnit d = attn::det_unit_of(u, n_heads, n, group, descending);
+    unit_head[u] = d.bh;
+    unit_key_tile[u] = d.j;
+    int* row = rank + (size_t)u * n;
+    if (rotated) {
+      const attn::DetRot r = attn::det_rot(u, n_ctas, n_heads, n, group, descending);
+      unit_first_tile[u] = attn::det_rot_first(r.jj, n, r.sigma);
+      for (int i = 0; i < n; ++i) row[i] = attn::det_rot_rank(i, r, n);
+    } else {
+      unit_first_tile[u] = n - 1;
+      for (int i = 0; i < n; ++i) row[i] = (causal && i < d.j) ? -1 : attn::det_rank(i, d.j, n, causal != 0, descending);
+    }
+  }
+  return ATTN_OK;
+}
+
 int attn_set_exp_poly(int enable) {
   if (enable != 0 && enable != 1) return ATTN_ERR_INVALID_ARG;
   settings();
@@ -651,24 +678,34 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if (int st = make_map(&p.tm_do, dO, BH, N, d_v)) return st;
   p.h_q = H;
   p.kv_group = H / H_kv;
-  {
-    const int n_heads = B * H_kv;  // the units' heads (K/V heads)
-    // measured on GB300 (H = 16, d = 128): 8-head groups are 4-5 % faster
-    // than one all-head group without a mask on the one-unit kernel (N >=
-    // 4096); on the persistent kernel (N <= 2048) and under the causal mask
-    // one group over all heads, longest key tiles first, is the fastest
-    const bool persistent_det = N <= 2048;  // the deterministic backward's kernel choice below
-    const int g = cfg.det_group > 0 ? cfg.det_group : ((causal || persistent_det) ? n_heads : 8);
-    p.det_group = g < n_heads ? g : n_heads;
-    p.det_desc = mask != nullptr ? 0 : cfg.det_desc;
-  }
   // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)
   p.pair_mode = (d_qk == 128 && cfg.bwd_pair && mask == nullptr && !gqa) ? 1 : 0;
   if (mask != nullptr) p.mask = *mask;
   // persistent CTAs when the (head, key tile) units are short (measured on
-  // GB300: +5-15 % at N <= 2048; at N = 4096 +1-5 % with atomic dQ and
-  // mixed with tickets; slower at N = 16384)
-  p.persist = cfg.bwd_persist >= 0 ? cfg.bwd_persist : ((N <= 2048 || (N <= 4096 && !deterministic)) ? 1 : 0);
+  // GB300: +5-15 % at N <= 2048; at N = 4096 +1-5 % with atomic dQ; 1.5 %
+  // slower at N = 16384), and for the deterministic mode without the causal
+  // mask at every N (d = 128: its rotated walk, +1-4 % at N >= 8192, +5-24 %
+  // below, over the one-unit kernel's best order).  d_qk = 64 and 128 have
+  // a persistent kernel, without grouped-query heads or masks.
+  const bool det_rotated = deterministic && !causal && mask == nullptr && !gqa && d_qk == 128;
+  p.persist = cfg.bwd_persist >= 0 ? cfg.bwd_persist
+                                   : ((N <= 2048 || (N <= 4096 && !deterministic) || det_rotated) ? 1 : 0);
+  {
+    const int n_heads = B * H_kv;  // the units' heads (K/V heads)
+    const bool persistent_kernel = p.persist && !p.pair_mode && d_qk <= 128 && mask == nullptr && !gqa;
+    // measured on GB300 (H = 16, d = 128): the persistent kernel without the
+    // causal mask (its rotated walk) is fastest with one-head groups for
+    // N <= 2048 and one group of all heads above; the one-unit kernel
+    // without a mask with 8-head groups for N > 2048 (4-5 % over one
+    // all-head group); under the causal mask, and for short sequences on the
+    // one-unit kernel, one group over all heads, longest key tiles first
+    const int g = cfg.det_group > 0              ? cfg.det_group
+                  : (persistent_kernel && !causal) ? (N <= 2048 ? 1 : n_heads)
+                  : (causal || N <= 2048)           ? n_heads
+                                                    : 8;
+    p.det_group = g < n_heads ? g : n_heads;
+    p.det_desc = mask != nullptr ? 0 : cfg.det_desc;
+  }
   if (p.pair_mode) {
     if (int st = make_map(&p.tm_q_half, q, BH, N, d_qk, 64)) return st;
     if (int st = make_map(&p.tm_do_half, dO, BH, N, d_v, 64)) return st;

@@ -41,6 +41,7 @@
 #include <type_traits>
 
 #include "attn_mask.cuh"
+#include "det_order.h"
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -131,29 +132,11 @@ __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Deterministic mode's order of the (head, key tile) work units: key-tile-
-// major inside groups of ``group`` heads (the heads of a group interleaved),
-// key tiles ascending, or from the last down with ``desc``.  Every dQ tile
-// takes its key-tile contributions in that same order (det_rank), so a unit
-// waits only on units of its own head that come earlier in the order: with
-// CTAs launched (or persistent CTAs taking units) in increasing order, the
-// waits always point backwards.  group = all heads keeps each head's key
-// tiles close in time (short ticket chains) but spreads the resident CTAs'
-// dQ additions over every head's accumulator; small groups do the opposite.
+// Deterministic mode's unit order and ticket ranks: det_order.h.
 __device__ __forceinline__ void det_unit(int u, int n_heads, int n, int group, int desc, int& j, int& bh) {
-  const int grp = u / (group * n);
-  const int h0 = grp * group;
-  const int g = min(group, n_heads - h0);  // heads in this (possibly last, smaller) group
-  const int rem = u - h0 * n;
-  const int jj = rem / g;
-  bh = h0 + (rem - jj * g);
-  j = desc ? n - 1 - jj : jj;
-}
-
-// Position of key tile j among the contributions to query tile i (the ticket
-// value at which its dQ addition may go ahead).
-__device__ __forceinline__ int det_rank(int i, int j, int n, bool causal, int desc) {
-  return desc ? (causal ? i : n - 1) - j : j;
+  const DetUnit d = det_unit_of(u, n_heads, n, group, desc);
+  j = d.j;
+  bh = d.bh;
 }
 
 // -------------------------------------------------------------- preprocess

@@ -57,7 +57,11 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
   // Causal key tiles with small j are the longest and go first in either
   // order.  GQA: walk position qi = g * n + i over query head g of the group
   // and query tile i (from n-1 down to i_lo, head after head); the first
-  // query head of K/V head bh is qh0.
+  // query head of K/V head bh is qh0.  Deterministic and non-causal: the
+  // rotated walk of det_order.h (every CTA is resident, the kernel being
+  // launched cooperatively), unit jj starting at query tile
+  // (n - 1 - sigma jj) mod n and wrapping from 0 to n - 1.
+  constexpr bool kRot = DETERMINISTIC && !CAUSAL && !MASK && !GQA;
   struct BUnit {
     int j, bh, i_lo, n_it, qh0, i_first;
   };
@@ -83,12 +87,17 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
     }
     // every role walks the same query tiles, from the last down
     w.i_first = MASK ? mask_prev_query_tile(p.mask, w.j, n) : n - 1;
+    if (kRot) {
+      const DetRot d = det_rot(u, (int)gridDim.x, n_heads, n, p.det_group, p.det_desc);
+      w.i_first = det_rot_first(d.jj, n, d.sigma);
+    }
     return w;
   };
   auto tile_i = [&](int qi) { return GQA ? qi % n : qi; };
   auto head_q = [&](const BUnit& w, int qi) { return GQA ? w.qh0 + qi / n : w.bh; };
   auto i_next = [&](const BUnit& w, int i) {
     if (GQA) return (i % n) > w.i_lo ? i - 1 : (i / n + 1) * n + (n - 1);
+    if (kRot) return i > 0 ? i - 1 : n - 1;
     return MASK ? mask_prev_query_tile(p.mask, w.j, i) : i - 1;
   };
   // persistent CTAs take unit r G + b in round r (G - 1 - b on odd rounds, so
@@ -314,6 +323,7 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
         if (PERSIST && u >= n_units) continue;
         const BUnit w = unit_at(u);
         const int j = w.j;
+        const DetRot dr = kRot ? det_rot(u, (int)gridDim.x, n_heads, n, p.det_group, p.det_desc) : DetRot{};
         for (int it = 0, qi = w.i_first; ok && it < w.n_it; ++it, qi = i_next(w, qi)) {
           const int tt = t + it;
           if ((tt & 1) != wr) continue;
@@ -321,13 +331,13 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
           const int qh = head_q(w, qi);
           float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(D * kBTile);
           int* ticket = p.tickets + (size_t)qh * p.n_tiles + i;
+          const int rank = kRot ? det_rot_rank(i, dr, n) : det_rank(i, j, n, CAUSAL, p.det_desc);
           constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
           for (int r = 0; ok && r < L::kStgRounds; ++r) {
             if (!(ok = mbar_wait(bar(L::kBarStgFull + wr), seen & 1, ctl, kBWhereDq + 2))) break;
             ++seen;
             if (r == 0) {
               const uint64_t t0 = globaltimer_ns();
-              const int rank = det_rank(i, j, n, CAUSAL, p.det_desc);
               while (ld_acquire_gpu(ticket) != rank) {
                 if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
                   if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);

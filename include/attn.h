@@ -370,7 +370,8 @@ int attn_set_bwd_pair(int enable);
  * mode = 1 runs the persistent kernel (one CTA per SM taking the (head, key
  * tile) units in rounds), 0 the kernel with one CTA per unit, -1 (the
  * default; also ATTN_BWD_PERSIST at first use) chooses by size: persistent for
- * N <= 2048, and for N <= 4096 in atomic mode.  Results meet the same
+ * N <= 2048, for N <= 4096 in atomic mode, and at every N for the
+ * deterministic mode without the causal mask at d = 128.  Results meet the same
  * tolerances either way; deterministic mode is bit-identical run to run with
  * either kernel (the two may differ from each other in the last bits).
  * Applies to d_qk = d_v = 64 and 128 without grouped-query heads or masks;
@@ -391,13 +392,20 @@ int attn_set_bwd_persist(int mode);
  * backward -- head swizzle, shortest- or longest-first, reverse m-block
  * order).  The (head, key tile) units run key-tile-major inside groups of
  * ``head_group`` heads (0, the default, picks the fastest order measured on
- * GB300: groups of 8 heads without a causal mask for N > 2048, one group of
- * all heads otherwise; also ATTN_DET_GROUP at first use); ``descending`` = 1
- * (ATTN_DET_DESC) takes the
+ * GB300: without a causal mask, on the persistent kernel groups of one head
+ * for N <= 2048 and one group of all heads above, on the one-unit kernel
+ * (d_qk = 192) one group of all heads for N <= 2048 and groups of 8 heads
+ * above; under the causal mask one group of all heads; also ATTN_DET_GROUP
+ * at first use); ``descending`` = 1 (ATTN_DET_DESC) takes the
  * key tiles from the last down -- shortest first under the causal mask --
  * and every dQ tile then adds its key-tile contributions in that same
  * descending order, 0 ascending (longest first under the causal mask).
- * Query tiles are always visited from the last down.  Each setting is
+ * The one-unit kernel and the causal mask visit the query tiles from the last
+ * down; the persistent kernel without the causal mask (the default for
+ * d = 128 at every N, and for N <= 2048) rotates each round's walks so that
+ * a head's units start at different query tiles, and a dQ tile takes the
+ * additions of a round in the order of their visits (attn_bwd_det_plan
+ * writes the plan out).  Each setting is
  * bit-reproducible on its own; different settings add in different orders
  * and may differ from each other in the last bits.  Applies to later
  * deterministic attn_bwd / attn_bwd_gqa / attn_bwd_noalloc calls except the
@@ -405,6 +413,29 @@ int attn_set_bwd_persist(int mode);
  * or ATTN_ERR_INVALID_ARG (head_group < 0, descending not 0 or 1).
  */
 int attn_set_det_schedule(int head_group, int descending);
+
+/*
+ * The deterministic backward's plan, as its kernels compute it, written out
+ * for host-side checks (no GPU work).  For n_heads heads of n_tiles 128-row
+ * tiles taken by n_ctas persistent CTAs in units of head_group heads
+ * (clipped to n_heads) and the order ``descending`` (attn_set_det_schedule):
+ * unit u (0 .. n_heads * n_tiles - 1, the launch / round order) is key tile
+ * unit_key_tile[u] of head unit_head[u]; it visits the query tiles from
+ * unit_first_tile[u] downwards, wrapping from 0 to n_tiles - 1 (rotated) or
+ * ending at 0 (the key tile under the causal mask); and its addition to dQ
+ * tile i goes ahead when that tile's ticket reaches rank[u * n_tiles + i]
+ * (-1: the unit does not touch tile i).  ``rotated`` = 1 gives the walk of
+ * the persistent non-causal kernel (every CTA resident at once): in each
+ * round of n_ctas units the units of one head start at different query
+ * tiles ("FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
+ * Asymmetric Hardware Scaling", Figures 7-8, on the deterministic schedule).
+ * Arrays are caller-owned host memory of n_heads * n_tiles ints (rank:
+ * n_heads * n_tiles * n_tiles).  Returns ATTN_OK or ATTN_ERR_INVALID_ARG
+ * (sizes < 1, flags not 0/1, rotated with causal, null arrays, more than
+ * 2^28 ranks).
+ */
+int attn_bwd_det_plan(int n_heads, int n_tiles, int n_ctas, int head_group, int descending, int causal, int rotated,
+                      int* unit_head, int* unit_key_tile, int* unit_first_tile, int* rank);
 
 /*
  * Per-kernel timing for benchmarks.  Between attn_profile_start and

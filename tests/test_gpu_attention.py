@@ -449,6 +449,35 @@ def test_deterministic_schedules(A, group, desc, causal, persist):
         G.assert_grad_close(name, G.f64(got), ref)
 
 
+@pytest.mark.parametrize("N,group,desc", [(1024, 4, 0), (1000, 1, 1), (1024, 0, 0), (4096, 8, 0)])
+def test_deterministic_rotated_rounds(A, N, group, desc):
+    """The persistent deterministic backward over more (head, key tile) units
+    than CTAs, so that CTAs take several rounds: without the causal mask the
+    units of a head in one round start at different query tiles (the rotated
+    walk; group = 0 at these sizes puts one unit of a head in a round, the
+    plain walk).  Bit-identical over repeats; gradients of sampled heads
+    against the oracle."""
+    torch = G.torch_mod()
+    B, H, d = 2, 16, 128
+    t = G.inputs(B, H, N, d, d, seed=47)
+    o, lse = G.run_fwd(A, t, 0)
+    A.attn_set_det_schedule(group, desc)
+    A.attn_set_bwd_persist(1)
+    try:
+        runs = [G.run_bwd(A, t, o, lse, 0, 1) for _ in range(2)]
+    finally:
+        A.attn_set_det_schedule(0, 0)
+        A.attn_set_bwd_persist(-1)
+    G.check_status(A)
+    for a, b in zip(*runs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for b, h in ((0, 0), (1, 15), (0, 9)):
+        q, k, v, do = (G.f64(t[n][b:b + 1, h:h + 1]) for n in ("q", "k", "v", "do"))
+        refs = ora.backward(q, k, v, do, 1.0 / math.sqrt(d), False)
+        for name, got, ref in zip(("dq", "dk", "dv"), runs[0], refs):
+            G.assert_grad_close(name, G.f64(got[b:b + 1, h:h + 1]), ref)
+
+
 @pytest.mark.parametrize("group,desc", [(2, 1), (1, 0)])
 @pytest.mark.parametrize("causal", [0, 1])
 def test_deterministic_schedules_d192(A, group, desc, causal):
