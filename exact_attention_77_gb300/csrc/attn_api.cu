@@ -681,22 +681,23 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)
   p.pair_mode = (d_qk == 128 && cfg.bwd_pair && mask == nullptr && !gqa) ? 1 : 0;
   if (mask != nullptr) p.mask = *mask;
-  // persistent CTAs when the (head, key tile) units are short (measured on
-  // GB300: +5-15 % at N <= 2048; at N = 4096 +1-5 % with atomic dQ; 1.5 %
-  // slower at N = 16384), and for the deterministic mode without the causal
-  // mask at every N (d = 128: its rotated walk, +1-4 % at N >= 8192, +5-24 %
-  // below, over the one-unit kernel's best order).  d_qk = 64 and 128 have
-  // a persistent kernel, without grouped-query heads or masks.
-  const bool det_rotated = deterministic && !causal && mask == nullptr && !gqa && d_qk == 128;
-  p.persist = cfg.bwd_persist >= 0 ? cfg.bwd_persist
-                                   : ((N <= 2048 || (N <= 4096 && !deterministic) || det_rotated) ? 1 : 0);
+  // persistent CTAs when the (head, key tile) units are short: measured on
+  // GB300 (H = 16, d = 128), +5-15 % at N <= 2048 in both modes, +2-4 % at
+  // N = 4096 with atomic dQ (+2 % at N = 8192 without the causal mask), 3-6 %
+  // slower at N = 16384; with tickets the one-unit kernel is faster above
+  // N = 2048 (8-9 %) and the persistent one, on its rotated walk, below
+  // (+9-21 %).  d_qk = 64 and 128 have a persistent kernel, without
+  // grouped-query heads or masks.
+  p.persist = cfg.bwd_persist >= 0
+                  ? cfg.bwd_persist
+                  : ((N <= 2048 || (!deterministic && (N <= 4096 || (!causal && N <= 8192)))) ? 1 : 0);
   {
     const int n_heads = B * H_kv;  // the units' heads (K/V heads)
     const bool persistent_kernel = p.persist && !p.pair_mode && d_qk <= 128 && mask == nullptr && !gqa;
     // measured on GB300 (H = 16, d = 128): the persistent kernel without the
     // causal mask (its rotated walk) is fastest with one-head groups for
     // N <= 2048 and one group of all heads above; the one-unit kernel
-    // without a mask with 8-head groups for N > 2048 (4-5 % over one
+    // without a mask with 8-head groups for N > 2048 (1-4 % over one
     // all-head group); under the causal mask, and for short sequences on the
     // one-unit kernel, one group over all heads, longest key tiles first
     const int g = cfg.det_group > 0              ? cfg.det_group

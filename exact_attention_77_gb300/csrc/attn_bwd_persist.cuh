@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
         cnt = 256;  // both compute warpgroups
       if (b == L::kBarDQFree) cnt = 128;  // the dQ warpgroup
       if (b == L::kBarAccFree) cnt = 256;  // both compute warpgroups
-      if (b == L::kBarStgFull || b == L::kBarStgFull + 1) cnt = 4;  // the dQ warpgroup's warps
+      if (b >= L::kBarStgFull && b < L::kBarStgFull + 4) cnt = 4;  // the dQ warpgroup's warps
       mbar_init(bar(b), cnt);
     }
     *abort_flag = 0;
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
     // additions are complete, overlapping that wait with the other reducer.
     if (lane == 0) {
       const int wr = warp - 2;
-      uint32_t seen = 0;  // completed phases of this reducer's staging barrier
+      int kt = 0;  // tiles this reducer has taken
       bool ok = true;
       int t = 0;  // tiles of earlier units
       for (int rd = 0; ok && rd < n_rounds; ++rd) {
@@ -332,10 +332,11 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
           float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(D * kBTile);
           int* ticket = p.tickets + (size_t)qh * p.n_tiles + i;
           const int rank = kRot ? det_rot_rank(i, dr, n) : det_rank(i, j, n, CAUSAL, p.det_desc);
-          constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
-          for (int r = 0; ok && r < L::kStgRounds; ++r) {
-            if (!(ok = mbar_wait(bar(L::kBarStgFull + wr), seen & 1, ctl, kBWhereDq + 2))) break;
-            ++seen;
+          constexpr int kRoundFloats = L::kSlotBytes / 4;
+          for (int r = 0; ok && r < L::kRounds; ++r) {
+            const int sl = r & 1;
+            const uint32_t par = (uint32_t)(kt * (L::kRounds / 2) + (r >> 1)) & 1;
+            if (!(ok = mbar_wait(bar(L::kBarStgFull + 2 * wr + sl), par, ctl, kBWhereDq + 2))) break;
             if (r == 0) {
               const uint64_t t0 = globaltimer_ns();
               while (ld_acquire_gpu(ticket) != rank) {
@@ -349,13 +350,18 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
               if (*ctl.abort) ok = false;
             }
             if (!ok) break;
-            bulk_reduce_add_f32(gdst + (size_t)r * kGroupsPerRound * kBTile * 4, sbase + L::kStgOff,
-                                L::kStgBytes);
+            bulk_reduce_add_f32(gdst + (size_t)r * kRoundFloats, sbase + L::kStgOff + sl * L::kSlotBytes,
+                                L::kSlotBytes);
             bulk_commit();
-            bulk_wait_read<0>();
-            mbar_arrive(bar(L::kBarStgFree));  // the staging tile may be overwritten
+            if (r > 0) {  // the previous round's slot has been read: it may be overwritten
+              bulk_wait_read<1>();
+              mbar_arrive(bar(L::kBarStgFree + (sl ^ 1)));
+            }
           }
           if (!ok) break;
+          bulk_wait_read<0>();
+          mbar_arrive(bar(L::kBarStgFree + ((L::kRounds - 1) & 1)));
+          ++kt;
           bulk_wait_all<0>();  // the additions are performed before the next key tile's
           fence_proxy_async_global();
           red_release_gpu_add(ticket, 1);
@@ -606,80 +612,63 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 15);
       // Stage the tile in shared memory in the accumulator's [D/4 column
       // groups][128 rows][4] order (each thread's 16-byte stores land side by
-      // side with its neighbours'), then one thread hands it to the copy
-      // engine as a bulk FP32 reduce-add.  The staging tile is reused once
-      // the previous tile's bulk read of it has finished.
+      // side with its neighbours') round by round through the two-slot ring,
+      // and the copy engine adds each round into the FP32 accumulator as a
+      // bulk reduce-add.
       float* stg = reinterpret_cast<float*>(smem + L::kStgOff);
-      constexpr int kGroupsPerRound = D / 4 / L::kStgRounds;
+      constexpr int kRoundGroups = D / 4 / L::kRounds;
       if constexpr (DETERMINISTIC) {
         // the reducer warps issue the additions in ticket order; each round is
-        // staged once the previous round has been read
+        // staged into its ring slot once the slot's previous round has been read
 #pragma unroll
-        for (int r = 0; r < L::kStgRounds && ok; ++r) {
-          const int g_round = tt * L::kStgRounds + r;  // staging rounds so far
-          if (g_round > 0)
+        for (int r = 0; r < L::kRounds && ok; ++r) {
+          const int sl = r & 1;
+          const int use = (tt * L::kRounds + r) >> 1;  // earlier rounds through this slot
+          if (use > 0)
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(bar(L::kBarStgFree), (uint32_t)(g_round - 1) & 1, ctl, kBWhereDq + 1));
+                            mbar_wait(bar(L::kBarStgFree + sl), (uint32_t)(use - 1) & 1, ctl, kBWhereDq + 1));
           if (!ok) break;
+          float* slot = stg + sl * (L::kSlotBytes / 4);
 #pragma unroll
-          for (int g = 0; g < kGroupsPerRound; ++g) {
-            const int gg = r * kGroupsPerRound + g;
-            *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+          for (int g = 0; g < kRoundGroups; ++g) {
+            const int gg = r * kRoundGroups + g;
+            *reinterpret_cast<float4*>(slot + (g * kBTile + qrow) * 4) =
                 make_float4(dq[4 * gg], dq[4 * gg + 1], dq[4 * gg + 2], dq[4 * gg + 3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::kBarStgFull + (tt & 1)));
+          if (lane == 0) mbar_arrive(bar(L::kBarStgFull + 2 * (tt & 1) + sl));
         }
         if (!ok) break;
         continue;
       }
+      // atomic mode: this warpgroup issues the reduce-adds itself; a round is
+      // staged into its ring slot once the slot's previous round has been
+      // read (all but the newest bulk group complete), while the copy engine
+      // still reads the other slot
       float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(D * kBTile);
-      int* ticket = DETERMINISTIC ? p.tickets + (size_t)qh * p.n_tiles + i : nullptr;
 #pragma unroll
-      for (int r = 0; r < L::kStgRounds; ++r) {
-        if (tt > 0 || r > 0) {  // the previous round's bulk read of the staging tile
-          if (tid == 0) bulk_wait_read<0>();
+      for (int r = 0; r < L::kRounds; ++r) {
+        const int sl = r & 1;
+        if (tt > 0 || r > 1) {
+          if (tid == 0) bulk_wait_read<1>();
           __syncwarp();
           named_bar_sync(1, 128);
         }
+        float* slot = stg + sl * (L::kSlotBytes / 4);
 #pragma unroll
-        for (int g = 0; g < kGroupsPerRound; ++g) {
-          const int gg = r * kGroupsPerRound + g;
-          *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+        for (int g = 0; g < kRoundGroups; ++g) {
+          const int gg = r * kRoundGroups + g;
+          *reinterpret_cast<float4*>(slot + (g * kBTile + qrow) * 4) =
               make_float4(dq[4 * gg], dq[4 * gg + 1], dq[4 * gg + 2], dq[4 * gg + 3]);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        if (tid == 0) {
-          if (DETERMINISTIC && r == 0) {
-            const uint64_t t0 = globaltimer_ns();
-            // tile i takes its (visible) key tiles in ascending order
-            int rank = det_rank(i, j, n, CAUSAL, p.det_desc);
-            if (MASK) {
-              rank = 0;
-              for (int jj = 0; jj < j; ++jj) rank += mask_tile_visible(p.mask, i, jj) ? 1 : 0;
-            }
-            while (ld_acquire_gpu(ticket) != rank) {
-              if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
-                if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
-                *ctl.abort = 1;
-                break;
-              }
-            }
-            fence_proxy_async_global();
-          }
-          if (!*ctl.abort) {
-            bulk_reduce_add_f32(gdst + (size_t)r * kGroupsPerRound * kBTile * 4, smem_u32(stg), L::kStgBytes);
-            bulk_commit();
-          }
+        if (tid == 0 && !*ctl.abort) {
+          bulk_reduce_add_f32(gdst + (size_t)r * (L::kSlotBytes / 4), smem_u32(slot), L::kSlotBytes);
+          bulk_commit();
         }
         __syncwarp();  // lane 0 rejoins its warp before the next (aligned) named barrier
-      }
-      if (DETERMINISTIC && tid == 0) {
-        bulk_wait_all<0>();  // the additions are performed before the next key tile's
-        fence_proxy_async_global();
-        if (!*ctl.abort) red_release_gpu_add(ticket, 1);
       }
       __syncwarp();
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 11);

@@ -370,8 +370,8 @@ int attn_set_bwd_pair(int enable);
  * mode = 1 runs the persistent kernel (one CTA per SM taking the (head, key
  * tile) units in rounds), 0 the kernel with one CTA per unit, -1 (the
  * default; also ATTN_BWD_PERSIST at first use) chooses by size: persistent for
- * N <= 2048, for N <= 4096 in atomic mode, and at every N for the
- * deterministic mode without the causal mask at d = 128.  Results meet the same
+ * N <= 2048, and in atomic mode also for N <= 4096 (N <= 8192 without the
+ * causal mask).  Results meet the same
  * tolerances either way; deterministic mode is bit-identical run to run with
  * either kernel (the two may differ from each other in the last bits).
  * Applies to d_qk = d_v = 64 and 128 without grouped-query heads or masks;
@@ -394,15 +394,15 @@ int attn_set_bwd_persist(int mode);
  * ``head_group`` heads (0, the default, picks the fastest order measured on
  * GB300: without a causal mask, on the persistent kernel groups of one head
  * for N <= 2048 and one group of all heads above, on the one-unit kernel
- * (d_qk = 192) one group of all heads for N <= 2048 and groups of 8 heads
- * above; under the causal mask one group of all heads; also ATTN_DET_GROUP
- * at first use); ``descending`` = 1 (ATTN_DET_DESC) takes the
+ * one group of all heads for N <= 2048 and groups of 8 heads above; under
+ * the causal mask one group of all heads; also ATTN_DET_GROUP at first use);
+ * ``descending`` = 1 (ATTN_DET_DESC) takes the
  * key tiles from the last down -- shortest first under the causal mask --
  * and every dQ tile then adds its key-tile contributions in that same
  * descending order, 0 ascending (longest first under the causal mask).
  * The one-unit kernel and the causal mask visit the query tiles from the last
  * down; the persistent kernel without the causal mask (the default for
- * d = 128 at every N, and for N <= 2048) rotates each round's walks so that
+ * N <= 2048) rotates each round's walks so that
  * a head's units start at different query tiles, and a dQ tile takes the
  * additions of a round in the order of their visits (attn_bwd_det_plan
  * writes the plan out).  Each setting is
