@@ -46,9 +46,14 @@ struct Bwd192Layout {
   static constexpr int kDOOff = kQOff + kQKBytes;
   static constexpr int kDSOff = kDOOff + kVBytes;  // dS (bf16 128x128), MN-major for the dQ product
   static constexpr int kDSBytes = kBTile * kBTile * 2;
-  static constexpr int kStgOff = kDSOff + kDSBytes;  // dQ_i staging: 64 columns per round
+  // dQ_i staging: a ring of two 16 KiB slots; a tile goes through it in six
+  // rounds of 32 columns, round r in slot r % 2, so that one round is staged
+  // while the copy engine reads the other
+  static constexpr int kStgOff = kDSOff + kDSBytes;
   static constexpr int kStgBytes = 32 * 1024;
-  static constexpr int kStgRounds = kBTile * kDQK * 4 / kStgBytes;  // 3
+  static constexpr int kSlotBytes = kStgBytes / 2;
+  static constexpr int kRounds = kBTile * kDQK * 4 / kSlotBytes;  // 6
+  static constexpr int kRoundGroups = kSlotBytes / (kBTile * 16);  // 8 four-column groups
   static constexpr int kVecOff = kStgOff + kStgBytes;  // -LSE2[128], -D[128] fp32 of Q_i
   static constexpr int kVecBytes = 2 * kBTile * 4;
   static constexpr int kBarOff = kVecOff + kVecBytes;
@@ -65,12 +70,12 @@ struct Bwd192Layout {
   static constexpr int kBarDQFreeX = 13;   // 128 arrivals: dQ columns over X read
   static constexpr int kBarDQFreePK = 14;  // 128 arrivals: dQ columns over PK read
   static constexpr int kBarAccDone = 15;
-  // deterministic mode (as in bwd_kernel): + w: a staging round of a tile of
-  // reducer warp w is staged (4 dQ-warp arrivals); the staging tile has been
-  // read by the copy engine (1 arrival)
+  // deterministic mode (as in bwd_kernel): + 2 w + s: staging slot s holds a
+  // round of reducer warp w's tile (4 dQ-warp arrivals); + s: slot s has
+  // been read by the copy engine (1 arrival)
   static constexpr int kBarStgFull = 16;
-  static constexpr int kBarStgFree = 18;
-  static constexpr int kNumBars = 19;
+  static constexpr int kBarStgFree = 20;
+  static constexpr int kNumBars = 22;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       uint32_t cnt = 1;
       if (b == L::kBarPReady || b == L::kBarPReady + 1 || b == L::kBarDSFull || b == L::kBarDSFull + 1) cnt = 256;
       if (b == L::kBarDQFreeX || b == L::kBarDQFreePK) cnt = 128;
-      if (b == L::kBarStgFull || b == L::kBarStgFull + 1) cnt = 4;  // the dQ warpgroup's warps
+      if (b >= L::kBarStgFull && b < L::kBarStgFull + 4) cnt = 4;  // the dQ warpgroup's warps
       mbar_init(bar(b), cnt);
     }
     *abort_flag = 0;
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       // while the other reducer already serves the next tile.
       if (lane == 0) {
         const int w = warp - 2;
-        uint32_t seen = 0;  // completed phases of this reducer's staging barrier
+        int kt = 0;  // tiles this reducer has taken
         bool ok = true;
         for (int it = 0, qi = i_first; ok && it < n_it; ++it, qi = i_next(qi)) {
           if ((it & 1) != w) continue;
@@ -381,12 +386,14 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
           const int qh = head_q(qi);
           float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(DQK * kBTile);
           int* ticket = p.tickets + (size_t)qh * p.n_tiles + i;
-          for (int r = 0; ok && r < L::kStgRounds; ++r) {
-            if (!(ok = mbar_wait(bar(L::kBarStgFull + w), seen & 1, ctl, kB192WhereDq + 2))) break;
-            ++seen;
+          const int rank = det_rank(i, j, n, CAUSAL, p.det_desc);  // the fixed order
+          for (int r = 0; ok && r < L::kRounds; ++r) {
+            const int sl = r & 1;
+            const uint32_t par = (uint32_t)(kt * (L::kRounds / 2) + (r >> 1)) & 1;
+            if (!(ok = mbar_wait(bar(L::kBarStgFull + 2 * w + sl), par, ctl, kB192WhereDq + 2))) break;
             if (r == 0) {
               const uint64_t t0 = globaltimer_ns();
-              while (ld_acquire_gpu(ticket) != det_rank(i, j, n, CAUSAL, p.det_desc)) {  // the fixed order
+              while (ld_acquire_gpu(ticket) != rank) {
                 if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
                   if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
                   *ctl.abort = 1;
@@ -397,12 +404,18 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
               if (*ctl.abort) ok = false;
             }
             if (!ok) break;
-            bulk_reduce_add_f32(gdst + (size_t)r * 16 * kBTile * 4, sbase + L::kStgOff, L::kStgBytes);
+            bulk_reduce_add_f32(gdst + (size_t)r * (L::kSlotBytes / 4), sbase + L::kStgOff + sl * L::kSlotBytes,
+                                L::kSlotBytes);
             bulk_commit();
-            bulk_wait_read<0>();
-            mbar_arrive(bar(L::kBarStgFree));  // the staging tile may be overwritten
+            if (r > 0) {  // the previous round's slot has been read: it may be overwritten
+              bulk_wait_read<1>();
+              mbar_arrive(bar(L::kBarStgFree + (sl ^ 1)));
+            }
           }
           if (!ok) break;
+          bulk_wait_read<0>();
+          mbar_arrive(bar(L::kBarStgFree + ((L::kRounds - 1) & 1)));
+          ++kt;
           bulk_wait_all<0>();  // the additions are performed before the next key tile's
           fence_proxy_async_global();
           red_release_gpu_add(ticket, 1);
@@ -582,10 +595,10 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kDqRegs));
     // ========================== dQ warpgroup ===========================
-    // Round r stages dQ columns 64r .. 64r+63 in the accumulator's [48
+    // Round r stages dQ columns 32r .. 32r+31 in the accumulator's [48
     // groups][128 rows][4] order and has the copy engine add them.  Columns
     // 0 .. 127 (over X) are read first and released to the next tile's S^T;
-    // columns 128 .. 191 (over PK) after the first round.
+    // columns 128 .. 191 (over PK) after the first two rounds.
     const int quad = warp & 3;
     const int qrow = quad * 32 + lane;
     const int tid = threadIdx.x - 384;
@@ -602,53 +615,44 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 21);
       tc_fence_after();
       float* gdst = p.dq_acc + ((size_t)qh * p.n_tiles + i) * (size_t)(DQK * kBTile);
-      int* ticket = DETERMINISTIC ? p.tickets + (size_t)qh * p.n_tiles + i : nullptr;
-      // stage 16 column groups (64 columns) from v and hand them to the copy engine
-      auto round = [&](int r, const float* v) {
+      // stage round rr (32 columns, 8 four-column groups, from v) into ring
+      // slot rr % 2 and have the copy engine add it
+      auto round = [&](int rr, const float* v) {
+        const int sl = rr & 1;
+        float* slot = stg + sl * (L::kSlotBytes / 4);
         if constexpr (DETERMINISTIC) {
           // the reducer warps (above) issue the additions in ticket order;
-          // the round is staged once the previous round has been read
-          const int g_round = it * L::kStgRounds + r;
-          if (ok && g_round > 0)
+          // the round is staged once the slot's previous round has been read
+          const int use = (it * L::kRounds + rr) >> 1;  // earlier rounds through this slot
+          if (ok && use > 0)
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(bar(L::kBarStgFree), (uint32_t)(g_round - 1) & 1, ctl, kB192WhereDq + 1));
+                            mbar_wait(bar(L::kBarStgFree + sl), (uint32_t)(use - 1) & 1, ctl, kB192WhereDq + 1));
           if (!ok) return;
 #pragma unroll
-          for (int g = 0; g < 16; ++g)
-            *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+          for (int g = 0; g < L::kRoundGroups; ++g)
+            *reinterpret_cast<float4*>(slot + (g * kBTile + qrow) * 4) =
                 make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::kBarStgFull + (it & 1)));
+          if (lane == 0) mbar_arrive(bar(L::kBarStgFull + 2 * (it & 1) + sl));
           return;
         }
-        if (it > 0 || r > 0) {  // the previous round's bulk read of the staging tile
-          if (tid == 0) bulk_wait_read<0>();
+        // atomic: the slot's previous round has been read once all but the
+        // newest bulk group are complete
+        if (it > 0 || rr > 1) {
+          if (tid == 0) bulk_wait_read<1>();
           __syncwarp();
           named_bar_sync(1, 128);
         }
 #pragma unroll
-        for (int g = 0; g < 16; ++g)
-          *reinterpret_cast<float4*>(stg + (g * kBTile + qrow) * 4) =
+        for (int g = 0; g < L::kRoundGroups; ++g)
+          *reinterpret_cast<float4*>(slot + (g * kBTile + qrow) * 4) =
               make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        if (tid == 0) {
-          if (DETERMINISTIC && r == 0) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(ticket) != det_rank(i, j, n, CAUSAL, p.det_desc)) {  // the fixed order
-              if (*ctl.abort || globaltimer_ns() - t0 > ctl.timeout_ns) {
-                if (!*ctl.abort) report_error(ctl.status, ATTN_ERR_TIMEOUT, kBWhereTicket);
-                *ctl.abort = 1;
-                break;
-              }
-            }
-            fence_proxy_async_global();
-          }
-          if (!*ctl.abort) {
-            bulk_reduce_add_f32(gdst + (size_t)r * 16 * kBTile * 4, smem_u32(stg), L::kStgBytes);
-            bulk_commit();
-          }
+        if (tid == 0 && !*ctl.abort) {
+          bulk_reduce_add_f32(gdst + (size_t)rr * (L::kSlotBytes / 4), smem_u32(slot), L::kSlotBytes);
+          bulk_commit();
         }
         __syncwarp();
       };
@@ -659,12 +663,15 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       mbar_arrive(bar(L::kBarDQFreeX));
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 22);
       round(0, a);
+      round(1, a + 32);
       tmem_ld64(tDQ + 128, a);
       tc_fence_before();
       mbar_arrive(bar(L::kBarDQFreePK));
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 23);
-      round(1, b);
-      round(2, a);
+      round(2, b);
+      round(3, b + 32);
+      round(4, a);
+      round(5, a + 32);
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 24);
       if (DETERMINISTIC && !ok) break;
       __syncwarp();
