@@ -266,11 +266,12 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
             tma_load_3d(sbase + L::kDOOff + c * kBSub, &p.tm_do, c * 64, i * kBTile, qh, bar(L::kBarDOFull));
           issued_do = it + 1;
           // With one Q stage the next Q_i load sits on the critical path (it
-          // starts when this tile's dK product is done).  In deterministic
-          // mode, fetching its tiles into L2 a whole tile ahead measured 3-4 %
-          // faster on GB300; with atomic dQ 3 % slower (there the load waits
-          // behind the dQ reduce-adds, not on DRAM), so only there.
-          if (DETERMINISTIC && it + 1 < n_it) {
+          // starts when this tile's dK product is done): its tiles are
+          // fetched into L2 a whole tile ahead.  Measured on GB300: +3-4 %
+          // in deterministic mode; with atomic dQ 3 % slower while the dQ
+          // partials went through one 32 KiB staging tile, and 0-2 % faster
+          // since they go through the two-slot ring.
+          if (it + 1 < n_it) {
             const int qn = i_next(qi);
 #pragma unroll
             for (int c = 0; c < DQK / 64; ++c) tma_prefetch_l2_3d(&p.tm_q, c * 64, tile_i(qn) * kBTile, head_q(qn));
