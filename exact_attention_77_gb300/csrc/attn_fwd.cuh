@@ -307,26 +307,33 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
     auto issue_qk = [&](int t, int stage) {
       const uint64_t da = sdesc_sw128(sbase + t * L::kQBytes, 16, 1024);
       const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, 16, 1024);
+      if constexpr (!FP8) {  // statements of four products: one 64-column chunk each
+        constexpr int kC = kSubTile / 16;
+        static_assert(L::kQKSteps % 4 == 0 && L::kQKSteps <= 12, "K steps per S product");
+        mma_ss_x4<0, 2, 4, 6>(tmem + t * 256, da, db, kIdescQK, 0u);
+        if constexpr (L::kQKSteps >= 8) mma_ss_x4<kC, kC + 2, kC + 4, kC + 6>(tmem + t * 256, da, db, kIdescQK, 1u);
+        if constexpr (L::kQKSteps >= 12)
+          mma_ss_x4<2 * kC, 2 * kC + 2, 2 * kC + 4, 2 * kC + 6>(tmem + t * 256, da, db, kIdescQK, 1u);
+      } else {
 #pragma unroll
-      for (int kk = 0; kk < L::kQKSteps; ++kk) {
-        const uint32_t off = (kk / 4) * kSubTile + (kk % 4) * 32;
-        if constexpr (FP8)
+        for (int kk = 0; kk < L::kQKSteps; ++kk) {
+          const uint32_t off = (kk / 4) * kSubTile + (kk % 4) * 32;
           mma_ss_elect_f8(tmem + t * 256, sdesc_advance(da, off), sdesc_advance(db, off), kIdescQK, kk > 0);
-        else
-          mma_ss_elect(tmem + t * 256, sdesc_advance(da, off), sdesc_advance(db, off), kIdescQK, kk > 0);
+        }
       }
     };
     auto issue_pv = [&](int t, int stage, bool acc) {
       const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, kSubTile, 1024);
+      if constexpr (!FP8) {  // two statements of four products; A: P over 8 tensor-memory columns per step
+        static_assert(L::kPVSteps == 8, "K steps per P V product");
+        constexpr int kBS = L::kPVKeys * 128 / 16;
+        mma_ts_x4<0, kBS>(tmem + t * 256 + 128, tmem + t * 256, db, kIdescPV, acc ? 1u : 0u);
+        mma_ts_x4<4, kBS>(tmem + t * 256 + 128, tmem + t * 256, db, kIdescPV, 1u);
+      } else {
 #pragma unroll
-      for (int kk = 0; kk < L::kPVSteps; ++kk) {
-        // A: P over 8 tensor-memory columns per step; B: the step's kPVKeys V rows
-        if constexpr (FP8)
+        for (int kk = 0; kk < L::kPVSteps; ++kk)  // A: P over 8 tensor-memory columns per step; B: kPVKeys V rows
           mma_ts_elect_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * L::kPVKeys * 128),
                           kIdescPV, (acc || kk > 0) ? 1u : 0u);
-        else
-          mma_ts_elect(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, sdesc_advance(db, kk * L::kPVKeys * 128),
-                       kIdescPV, (acc || kk > 0) ? 1u : 0u);
       }
     };
     bool ok = true;

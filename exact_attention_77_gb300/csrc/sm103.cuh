@@ -281,31 +281,11 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // issuing lane chosen by a lane-index predicate, the issuing warp loses most
 // of its issue slots to the busy softmax warps on the same scheduler and the
 // tensor pipe runs dry; with elect.sync the forward went from about 1330 to
-// about 1700 TFLOP/s.
-__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same two forms for 8-bit floating-point operands (kind::f8f6f4; the
-// instruction descriptor gives their format, idesc_e4m3_f32).  One product
+// about 1700 TFLOP/s.  The bf16 forms (mma_ss_x4, mma_ts_x4) issue four
+// products per statement, below.
+//
+// One product per statement for 8-bit floating-point operands (kind::f8f6f4;
+// the instruction descriptor gives their format, idesc_e4m3_f32).  One product
 // covers K = 32 elements: 32 bytes of a K-major row, as for kind::f16.
 __device__ __forceinline__ void mma_ss_elect_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                 uint32_t accumulate) {
@@ -328,6 +308,56 @@ __device__ __forceinline__ void mma_ts_elect_f8(uint32_t d_tmem, uint32_t a_tmem
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four products in one statement with one elect.sync, for the issue loops
+// that the whole warp runs in step (fewer instructions per product than four
+// mma_*_elect calls; measured on GB300: forward +1-4 %).  SS form: both
+// descriptors' start fields moved by the same immediates O0..O3 (16-byte
+// units; the 14-bit start field cannot carry out for shared-memory
+// addresses, so the low word is added alone), the first product
+// accumulating when acc != 0 and the rest always.
+template <int O0, int O1, int O2, int O3>
+__device__ __forceinline__ void mma_ss_x4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, e;\n\t.reg .b32 al, ah, bl, bh, t0, t1;\n\t.reg .b64 x, y;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %9, 0;\n\t"
+      "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.u32 t0, al, %5;\n\tadd.u32 t1, bl, %5;\n\tmov.b64 x, {t0, ah};\n\tmov.b64 y, {t1, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, p;\n\t"
+      "add.u32 t0, al, %6;\n\tadd.u32 t1, bl, %6;\n\tmov.b64 x, {t0, ah};\n\tmov.b64 y, {t1, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n\t"
+      "add.u32 t0, al, %7;\n\tadd.u32 t1, bl, %7;\n\tmov.b64 x, {t0, ah};\n\tmov.b64 y, {t1, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n\t"
+      "add.u32 t0, al, %8;\n\tadd.u32 t1, bl, %8;\n\tmov.b64 x, {t0, ah};\n\tmov.b64 y, {t1, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc), "n"(O0), "n"(O1), "n"(O2), "n"(O3), "r"(1u)
+      : "memory");
+}
+
+// Four TS products in one statement: A from tensor memory at a_tmem + 8 k
+// (k = K0 .. K0+3), B's descriptor start field moved by BS * k.
+template <int K0, int BS>
+__device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, e;\n\t.reg .b32 bl, bh, t1, ta;\n\t.reg .b64 y;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %13, 0;\n\t"
+      "mov.b64 {bl, bh}, %2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.u32 ta, %1, %5;\n\tadd.u32 t1, bl, %9;\n\tmov.b64 y, {t1, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], y, %3, p;\n\t"
+      "add.u32 ta, %1, %6;\n\tadd.u32 t1, bl, %10;\n\tmov.b64 y, {t1, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], y, %3, q;\n\t"
+      "add.u32 ta, %1, %7;\n\tadd.u32 t1, bl, %11;\n\tmov.b64 y, {t1, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], y, %3, q;\n\t"
+      "add.u32 ta, %1, %8;\n\tadd.u32 t1, bl, %12;\n\tmov.b64 y, {t1, bh};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], y, %3, q;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc), "n"(8 * K0), "n"(8 * K0 + 8), "n"(8 * K0 + 16),
+      "n"(8 * K0 + 24), "n"(BS * K0), "n"(BS * K0 + BS), "n"(BS * K0 + 2 * BS), "n"(BS * K0 + 3 * BS), "r"(1u)
       : "memory");
 }
 
