@@ -372,11 +372,12 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
     } else if (DETERMINISTIC) {
       // ================= dQ reducers (deterministic mode) ==================
       // Warps 2 and 3 take the query tiles in turn: for each of the tile's
-      // three staged rounds the reducer waits for it, (first round) waits for
+      // six staged rounds the reducer waits for it, (first round) waits for
       // the tile's ticket, hands it to the copy engine as a bulk FP32
-      // reduce-add and frees the staging tile once read; after the last round
-      // it waits for the additions to complete and passes the ticket on,
-      // while the other reducer already serves the next tile.
+      // reduce-add and frees its ring slot once read (one round later, so
+      // the copy engine always has the next one queued); after the last
+      // round it waits for the additions to complete and passes the ticket
+      // on, while the other reducer already serves the next tile.
       if (lane == 0) {
         const int w = warp - 2;
         int kt = 0;  // tiles this reducer has taken
