@@ -188,28 +188,44 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdParams p) {
 }
 
 // ---------------------------------------------------------------- dQ out
-// Accumulator layout per (bh, tile): [D/4 groups][128 rows][4]; one warp per
-// row, lane g handles columns 4g..4g+3 (D = 128) or two lanes share (D = 64).
+// Accumulator layout per (bh, tile): [D/4 groups][128 rows][4] (pair mode:
+// [2 row halves][D/4][64][4]).  A thread takes one row and four consecutive
+// groups; a warp takes 32 consecutive rows of the same groups, so each of
+// its loads reads 512 contiguous bytes and each thread writes 32 contiguous
+// bytes of its dQ row (one whole sector).
 template <int D>
 __global__ void __launch_bounds__(256) dq_convert_kernel(BwdParams p) {
-  constexpr int kGroups = D / 4;                 // 32 or 16
-  constexpr int kRowsPerWarp = 32 / kGroups;      // 1 or 2
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const long row = (long)warp * kRowsPerWarp + lane / kGroups;
-  const int g = lane % kGroups;
-  if (row >= (long)p.BH * p.N) return;
-  const int bh = (int)(row / p.N);
-  const int i = (int)(row - (long)bh * p.N);
-  const int tile = i >> 7, r = i & 127;
-  // pair mode: each tile's accumulator is two [D/4][64][4] row halves
-  const size_t idx = p.pair_mode ? ((((size_t)bh * p.n_tiles + tile) * 2 + (r >> 6)) * kGroups + g) * 64 + (r & 63)
-                                 : (((size_t)bh * p.n_tiles + tile) * kGroups + g) * 128 + r;
-  const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + idx * 4);
-  uint2 out;
-  out.x = pack_bf16(a.x * p.scale, a.y * p.scale);
-  out.y = pack_bf16(a.z * p.scale, a.w * p.scale);
-  *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + (size_t)row * D + 4 * g) = out;
+  constexpr int kGroups = D / 4;    // 32 or 16
+  constexpr int kQuads = kGroups / 4;  // threads per row
+  const long x = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long per_tile = 128L * kQuads;
+  const long tile_g = x / per_tile;  // over BH * n_tiles
+  if (tile_g >= (long)p.BH * p.n_tiles) return;
+  const int tt = (int)(x - tile_g * per_tile);
+  const int w = tt >> 5;
+  const int r = (w & 3) * 32 + (threadIdx.x & 31);
+  const int q = w >> 2;
+  const int bh = (int)(tile_g / p.n_tiles);
+  const int tile = (int)(tile_g - (long)bh * p.n_tiles);
+  const int i = tile * 128 + r;
+  float4 a[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int g = 4 * q + k;
+    const size_t idx = p.pair_mode ? (((size_t)tile_g * 2 + (r >> 6)) * kGroups + g) * 64 + (r & 63)
+                                   : ((size_t)tile_g * kGroups + g) * 128 + r;
+    a[k] = *reinterpret_cast<const float4*>(p.dq_acc + idx * 4);
+  }
+  if (i >= p.N) return;
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    o[2 * k] = pack_bf16(a[k].x * p.scale, a[k].y * p.scale);
+    o[2 * k + 1] = pack_bf16(a[k].z * p.scale, a[k].w * p.scale);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + ((size_t)bh * p.N + i) * D + 16 * q);
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 // ---------------------------------------------------------------- main
@@ -846,8 +862,8 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
   }
   mark(2);
   {
-    const long warps = ((long)p.BH * p.N + (32 / (D / 4)) - 1) / (32 / (D / 4));
-    const long blocks = (warps * 32 + 255) / 256;
+    const long threads = (long)p.BH * p.n_tiles * 128 * (D / 16);
+    const long blocks = (threads + 255) / 256;
     dq_convert_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     mark(3);

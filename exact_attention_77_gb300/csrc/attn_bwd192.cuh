@@ -145,21 +145,35 @@ __global__ void __launch_bounds__(256) bwd192_pre_kernel(BwdParams p) {
 // in [48 column groups][128 rows][4] order.  One warp per row: lane g takes
 // groups g and, for g < 16, g + 32.
 __global__ void __launch_bounds__(256) dq192_convert_kernel(BwdParams p) {
-  constexpr int kGroups = Bwd192Layout::kDQK / 4;
-  const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= (long)p.BH * p.N) return;
-  const int bh = (int)(row / p.N);
-  const int i = (int)(row - (long)bh * p.N);
-  const size_t tile_base = ((size_t)bh * p.n_tiles + (i >> 7)) * kGroups;
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.dq) + (size_t)row * Bwd192Layout::kDQK;
-  for (int g = lane; g < kGroups; g += 32) {
-    const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + ((tile_base + g) * 128 + (i & 127)) * 4);
-    uint2 o;
-    o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
-    o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
-    *reinterpret_cast<uint2*>(out + 4 * g) = o;
+  // as dq_convert_kernel: one row and four consecutive column groups per
+  // thread, 32 consecutive rows of the same groups per warp
+  constexpr int kGroups = Bwd192Layout::kDQK / 4;  // 48
+  constexpr int kQuads = kGroups / 4;              // 12
+  const long x = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long per_tile = 128L * kQuads;
+  const long tile_g = x / per_tile;  // over BH * n_tiles
+  if (tile_g >= (long)p.BH * p.n_tiles) return;
+  const int tt = (int)(x - tile_g * per_tile);
+  const int w = tt >> 5;
+  const int r = (w & 3) * 32 + (threadIdx.x & 31);
+  const int q = w >> 2;
+  const int bh = (int)(tile_g / p.n_tiles);
+  const int i = (int)(tile_g - (long)bh * p.n_tiles) * 128 + r;
+  float4 a[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    a[k] = *reinterpret_cast<const float4*>(p.dq_acc + (((size_t)tile_g * kGroups + 4 * q + k) * 128 + r) * 4);
+  if (i >= p.N) return;
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    o[2 * k] = pack_bf16(a[k].x * p.scale, a[k].y * p.scale);
+    o[2 * k + 1] = pack_bf16(a[k].z * p.scale, a[k].w * p.scale);
   }
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) +
+                                        ((size_t)bh * p.N + i) * Bwd192Layout::kDQK + 16 * q);
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 template <bool CAUSAL, bool DETERMINISTIC, bool GQA>
@@ -716,7 +730,7 @@ cudaError_t launch_bwd192_instance(const BwdParams& p, cudaStream_t stream, cons
   }
   mark(2);
   {
-    const long blocks = ((long)p.BH * p.N * 32 + 255) / 256;  // one warp per row
+    const long blocks = ((long)p.BH * p.n_tiles * 128 * 12 + 255) / 256;  // 12 threads per row
     dq192_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     mark(3);
