@@ -706,6 +706,15 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
                                                     : 8;
     p.det_group = g < n_heads ? g : n_heads;
     p.det_desc = mask != nullptr ? 0 : cfg.det_desc;
+    // the first contribution (ticket 0) to each dQ tile as a plain store, the
+    // accumulator left unzeroed: measured on GB300 with the causal mask at
+    // d = 64 / 128, main kernel +1-4 % and call +2-7 % (N = 1024 .. 16384);
+    // the kernels take it in their causal instances only (in the others the
+    // branch alone cost the one-unit kernel 10 % at N = 16384), and the
+    // d_qk = 192 kernel not at all (mixed).  (Every dQ tile has a first
+    // contribution unless a mask map leaves it without any; grouped-query
+    // heads and CTA pairs add as before.)
+    p.acc_first_store = (deterministic && causal && d_qk <= 128 && mask == nullptr && !gqa && !p.pair_mode) ? 1 : 0;
   }
   if (p.pair_mode) {
     if (int st = make_map(&p.tm_q_half, q, BH, N, d_qk, 64)) return st;

@@ -176,8 +176,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdParams p) {
     p.row_d[row] = -acc;
     p.row_lse2[row] = i < p.N ? -p.lse[(size_t)bh * p.N + i] * 1.4426950408889634f : -INFINITY;
   }
-  // zero the dQ accumulator and the tickets (grid-stride, 16-byte stores)
-  const size_t n4 = (size_t)p.BH * p.Npad * D / 4;
+  // zero the dQ accumulator (unless each tile's first contribution is a
+  // store) and the tickets (grid-stride, 16-byte stores)
+  const size_t n4 = p.acc_first_store ? 0 : (size_t)p.BH * p.Npad * D / 4;
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
   for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += (size_t)gridDim.x * blockDim.x)
     acc4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -498,8 +499,11 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
             if (*ctl.abort) ok = false;
           }
           if (!ok) break;
-          bulk_reduce_add_f32(gdst + (size_t)r * kRoundFloats, sbase + L::kStgOff + sl * L::kSlotBytes,
-                              L::kSlotBytes);
+          if (CAUSAL && p.acc_first_store && rank == 0)  // the tile's first contribution (causal instances only)
+            bulk_store(gdst + (size_t)r * kRoundFloats, sbase + L::kStgOff + sl * L::kSlotBytes, L::kSlotBytes);
+          else
+            bulk_reduce_add_f32(gdst + (size_t)r * kRoundFloats, sbase + L::kStgOff + sl * L::kSlotBytes,
+                                L::kSlotBytes);
           bulk_commit();
           if (r > 0) {  // the previous round's slot has been read: it may be overwritten
             bulk_wait_read<1>();

@@ -142,8 +142,7 @@ __global__ void __launch_bounds__(256) bwd192_pre_kernel(BwdParams p) {
 }
 
 // dQ = scale * accumulator as bf16 [BH, N, 192]; accumulator per (bh, tile)
-// in [48 column groups][128 rows][4] order.  One warp per row: lane g takes
-// groups g and, for g < 16, g + 32.
+// in [48 column groups][128 rows][4] order.
 __global__ void __launch_bounds__(256) dq192_convert_kernel(BwdParams p) {
   // as dq_convert_kernel: one row and four consecutive column groups per
   // thread, 32 consecutive rows of the same groups per warp

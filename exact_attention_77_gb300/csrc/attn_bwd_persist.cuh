@@ -350,8 +350,11 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
               if (*ctl.abort) ok = false;
             }
             if (!ok) break;
-            bulk_reduce_add_f32(gdst + (size_t)r * kRoundFloats, sbase + L::kStgOff + sl * L::kSlotBytes,
-                                L::kSlotBytes);
+            if (CAUSAL && p.acc_first_store && rank == 0)  // the tile's first contribution (causal instances only)
+              bulk_store(gdst + (size_t)r * kRoundFloats, sbase + L::kStgOff + sl * L::kSlotBytes, L::kSlotBytes);
+            else
+              bulk_reduce_add_f32(gdst + (size_t)r * kRoundFloats, sbase + L::kStgOff + sl * L::kSlotBytes,
+                                  L::kSlotBytes);
             bulk_commit();
             if (r > 0) {  // the previous round's slot has been read: it may be overwritten
               bulk_wait_read<1>();

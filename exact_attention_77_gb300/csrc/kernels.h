@@ -99,6 +99,10 @@ struct BwdParams {
   // key tiles from the last down (and each dQ tile adds them in that order)
   int det_group;
   int det_desc;
+  // 1 (deterministic mode; chosen by the host): each dQ tile's first
+  // contribution (ticket 0) is a plain bulk store, so the preprocess leaves
+  // the FP32 accumulator unzeroed
+  int acc_first_store;
 };
 
 // Optional events recorded on the launch stream around each backward kernel:
