@@ -676,6 +676,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if (int st = make_map(&p.tm_k, k, B * H_kv, N, d_qk)) return st;
   if (int st = make_map(&p.tm_v, v, B * H_kv, N, d_v)) return st;
   if (int st = make_map(&p.tm_do, dO, BH, N, d_v)) return st;
+  if (int st = make_map(&p.tm_dk, dk, B * H_kv, N, d_qk)) return st;
+  if (int st = make_map(&p.tm_dv, dv, B * H_kv, N, d_v)) return st;
   p.h_q = H;
   p.kv_group = H / H_kv;
   // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)

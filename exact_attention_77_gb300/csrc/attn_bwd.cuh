@@ -671,15 +671,55 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
       }
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 7 + h);
     }
-    // epilogue: dV and dK rows of this key tile; warpgroup h writes columns
-    // [h*D/2, (h+1)*D/2)
+    // epilogue: dV and dK rows of this key tile.  Warpgroup h takes columns
+    // [h*D/2, (h+1)*D/2): each thread writes its key row into 64-column boxes
+    // in shared memory (the Q stages, free now: the last products have
+    // completed), in the 128-byte swizzled layout (16-byte unit c of row r at
+    // unit c ^ (r % 8)), then one thread has the copy engine store the boxes
+    // as whole rows (rows past N left out).
+    // (The deterministic instances keep direct row stores from registers:
+    // there the TMA epilogue measured 3-4 % slower at N = 16384.)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, ctl, kBWhereFin));
+    if constexpr (DETERMINISTIC) {
+      if (ok) {
+        tc_fence_after();
+        const size_t row = (size_t)bh * p.N + (key_dead ? 0 : k_glob);
+        uint4* dvrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dv) + row * D);
+        uint4* dkrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dk) + row * D);
+#pragma unroll
+        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+          float a[32], b[32];
+          if (n_it > 0) {
+            tmem_ld32(tmem + lane_base + L::kColDV + c0, a);
+            tmem_ld32(tmem + lane_base + L::kColDK + c0, b);
+          } else {  // (masked instance) no query sees this key tile: dK = dV = 0
+#pragma unroll
+            for (int q = 0; q < 32; ++q) a[q] = b[q] = 0.f;
+          }
+          uint32_t pa[16], pb[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            pa[q] = pack_bf16(a[2 * q], a[2 * q + 1]);
+            pb[q] = pack_bf16(b[2 * q] * p.scale, b[2 * q + 1] * p.scale);
+          }
+          if (!key_dead) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              dvrow[c0 / 8 + v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
+              dkrow[c0 / 8 + v] = make_uint4(pb[4 * v], pb[4 * v + 1], pb[4 * v + 2], pb[4 * v + 3]);
+            }
+          }
+        }
+      }
+    } else {
+    ok = named_bar_and(2, 256, ok);  // both compute warpgroups (the stores below need every row)
     if (ok) {
       tc_fence_after();
-      const bool live = !key_dead;
-      const size_t row = (size_t)bh * p.N + (live ? k_glob : 0);
-      uint4* dvrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dv) + row * D);
-      uint4* dkrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dk) + row * D);
+      constexpr int kBoxes = D / 64;          // per tensor
+      constexpr uint32_t kBoxBytes = kBTile * 128;
+      const uint32_t stg_dv = sbase + L::kQOff;
+      const uint32_t stg_dk = stg_dv + kBoxes * kBoxBytes;
+      static_assert(2 * kBoxes * kBoxBytes <= L::kQStages * L::kTileBytes, "dV / dK boxes fit the Q stages");
 #pragma unroll
       for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
         float a[32], b[32];
@@ -696,14 +736,26 @@ __global__ void __launch_bounds__(512, 1) bwd_kernel(const __grid_constant__ Bwd
           pa[q] = pack_bf16(a[2 * q], a[2 * q + 1]);
           pb[q] = pack_bf16(b[2 * q] * p.scale, b[2 * q + 1] * p.scale);
         }
-        if (live) {
+        const uint32_t box_off = (uint32_t)(c0 / 64) * kBoxBytes + (uint32_t)lrow * 128;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            dvrow[c0 / 8 + v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
-            dkrow[c0 / 8 + v] = make_uint4(pb[4 * v], pb[4 * v + 1], pb[4 * v + 2], pb[4 * v + 3]);
-          }
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t unit = (uint32_t)(((c0 % 64) / 8 + v) ^ (lrow & 7)) * 16;
+          st_shared_v4(stg_dv + box_off + unit, pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
+          st_shared_v4(stg_dk + box_off + unit, pb[4 * v], pb[4 * v + 1], pb[4 * v + 2], pb[4 * v + 3]);
         }
       }
+      fence_proxy_async_smem();
+      named_bar_sync(2, 256);
+      if (h == 0 && tid == 0) {
+#pragma unroll
+        for (int bx = 0; bx < kBoxes; ++bx) {
+          tma_store_3d(&p.tm_dv, stg_dv + bx * kBoxBytes, bx * 64, j * kBTile, bh);
+          tma_store_3d(&p.tm_dk, stg_dk + bx * kBoxBytes, bx * 64, j * kBTile, bh);
+        }
+        bulk_commit();
+        bulk_wait_read<0>();  // shared memory is read before the CTA exits
+      }
+    }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kDqRegs));

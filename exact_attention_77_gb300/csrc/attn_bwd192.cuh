@@ -577,16 +577,21 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
       if (!ok) break;
       if (tid == 0) ATTN_TRACE_AT(blockIdx.x, it, 19 + h);
     }
-    // epilogue: warpgroup h writes dV columns [64h, 64h+64) and dK columns
-    // [96h, 96h+96) of its key row
+    // epilogue: warpgroup h takes dV columns [64h, 64h+64) and dK columns
+    // [96h, 96h+96) of its key row, writes them into 64-column boxes in
+    // shared memory (the Q and dO stages, free now) in the 128-byte swizzled
+    // layout, and one thread has the copy engine store the boxes as whole
+    // rows (rows past N left out)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, ctl, kB192WhereEw + 4));
+    ok = named_bar_and(2, 256, ok);  // both compute warpgroups (the stores below need every row)
     if (ok) {
       tc_fence_after();
-      const bool live = !key_dead;
-      const size_t row = (size_t)bh * p.N + (live ? k_glob : 0);
-      uint4* dvrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dv) + row * DV);
-      uint4* dkrow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dk) + row * DQK);
-      auto write32 = [&](uint32_t col, uint4* dst, float mul) {
+      constexpr uint32_t kBoxBytes = kBTile * 128;
+      const uint32_t stg_dv = sbase + L::kQOff;                   // DV / 64 boxes
+      const uint32_t stg_dk = stg_dv + (DV / 64) * kBoxBytes;    // DQK / 64 boxes
+      static_assert(L::kDOOff == L::kQOff + L::kQKBytes && (DV + DQK) / 64 * kBoxBytes <= L::kQKBytes + L::kVBytes,
+                    "dV / dK boxes fit the Q and dO stages");
+      auto stage32 = [&](uint32_t col, uint32_t stg, int c0, float mul) {
         float a[32];
         if (n_it > 0) {
           tmem_ld32(tmem + lane_base + col, a);
@@ -597,15 +602,26 @@ __global__ void __launch_bounds__(512, 1) bwd192_kernel(const __grid_constant__ 
         uint32_t pa[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) pa[q] = pack_bf16(a[2 * q] * mul, a[2 * q + 1] * mul);
-        if (live) {
+        const uint32_t box_off = (uint32_t)(c0 / 64) * kBoxBytes + (uint32_t)lrow * 128;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
-        }
+        for (int v = 0; v < 4; ++v)
+          st_shared_v4(stg + box_off + (uint32_t)(((c0 % 64) / 8 + v) ^ (lrow & 7)) * 16, pa[4 * v], pa[4 * v + 1],
+                       pa[4 * v + 2], pa[4 * v + 3]);
       };
 #pragma unroll
-      for (int c0 = 64 * h; c0 < 64 * h + 64; c0 += 32) write32(L::kColDV + c0, dvrow + c0 / 8, 1.f);
+      for (int c0 = 64 * h; c0 < 64 * h + 64; c0 += 32) stage32(L::kColDV + c0, stg_dv, c0, 1.f);
 #pragma unroll
-      for (int c0 = 96 * h; c0 < 96 * h + 96; c0 += 32) write32(L::kColDK + c0, dkrow + c0 / 8, p.scale);
+      for (int c0 = 96 * h; c0 < 96 * h + 96; c0 += 32) stage32(L::kColDK + c0, stg_dk, c0, p.scale);
+      fence_proxy_async_smem();
+      named_bar_sync(2, 256);
+      if (h == 0 && tid == 0) {
+#pragma unroll
+        for (int bx = 0; bx < DV / 64; ++bx) tma_store_3d(&p.tm_dv, stg_dv + bx * kBoxBytes, bx * 64, j * kBTile, bh);
+#pragma unroll
+        for (int bx = 0; bx < DQK / 64; ++bx) tma_store_3d(&p.tm_dk, stg_dk + bx * kBoxBytes, bx * 64, j * kBTile, bh);
+        bulk_commit();
+        bulk_wait_read<0>();  // shared memory is read before the CTA exits
+      }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kDqRegs));

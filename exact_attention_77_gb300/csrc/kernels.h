@@ -67,6 +67,8 @@ struct BwdParams {
   CUtensorMap tm_k;   // [BH, N, d_qk]
   CUtensorMap tm_v;   // [BH, N, d_v]
   CUtensorMap tm_do;  // [BH, N, d_v]
+  CUtensorMap tm_dk;  // [BH_kv, N, d_qk] bf16 output (the one-CTA kernels' TMA stores)
+  CUtensorMap tm_dv;  // [BH_kv, N, d_v]
   CUtensorMap tm_q_half;   // Q with 64-row boxes (CTA-pair backward)
   CUtensorMap tm_do_half;  // dO with 64-row boxes (CTA-pair backward)
   const void* o;      // bf16 [BH, N, d_v]
