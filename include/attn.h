@@ -370,8 +370,8 @@ int attn_set_bwd_pair(int enable);
  * mode = 1 runs the persistent kernel (one CTA per SM taking the (head, key
  * tile) units in rounds), 0 the kernel with one CTA per unit, -1 (the
  * default; also ATTN_BWD_PERSIST at first use) chooses by size: persistent for
- * N <= 2048, and in atomic mode also for N <= 4096 (N <= 8192 without the
- * causal mask).  Results meet the same
+ * N <= 2048, and in atomic mode at every N without the causal mask and for
+ * N <= 8192 with it.  Results meet the same
  * tolerances either way; deterministic mode is bit-identical run to run with
  * either kernel (the two may differ from each other in the last bits).
  * Applies to d_qk = d_v = 64 and 128 without grouped-query heads or masks;
