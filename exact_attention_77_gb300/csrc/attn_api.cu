@@ -683,16 +683,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // d = 128 runs the CTA-pair main kernel when enabled (attn_set_bwd_pair)
   p.pair_mode = (d_qk == 128 && cfg.bwd_pair && mask == nullptr && !gqa) ? 1 : 0;
   if (mask != nullptr) p.mask = *mask;
-  // persistent CTAs (measured on GB300, H = 16, d = 128, with their TMA
-  // epilogue): with atomic dQ at every N without the causal mask (+3.7 % at
-  // N = 16384, +3.5 % at 8192, more below) and up to N = 8192 with it (+4 %
-  // at 8192; 5 % slower at 16384); with tickets for N <= 2048, where its
-  // rotated walk beats the one-unit kernel's best order by 9-21 % (the one-
-  // unit kernel is 8-9 % faster above).  d_qk = 64 and 128 have a persistent
-  // kernel, without grouped-query heads or masks.
-  p.persist = cfg.bwd_persist >= 0
-                  ? cfg.bwd_persist
-                  : ((N <= 2048 || (!deterministic && (!causal || N <= 8192))) ? 1 : 0);
+  // persistent CTAs (measured on GB300, H = 16, with their TMA epilogue):
+  // with atomic dQ at every N (d = 128 without the causal mask +3.7 % at
+  // N = 16384 and +3.5 % at 8192; with it +6 % at 16384 and +10-16 % at
+  // 8192 .. 2048; d = 64 with it +9-16 %); with tickets for N <= 2048, where
+  // its rotated walk beats the one-unit kernel's best order by 9-21 % (the
+  // one-unit kernel is 8-9 % faster above).  d_qk = 64 and 128 have a
+  // persistent kernel, without grouped-query heads or masks.
+  p.persist = cfg.bwd_persist >= 0 ? cfg.bwd_persist : ((N <= 2048 || !deterministic) ? 1 : 0);
   {
     const int n_heads = B * H_kv;  // the units' heads (K/V heads)
     const bool persistent_kernel = p.persist && !p.pair_mode && d_qk <= 128 && mask == nullptr && !gqa;

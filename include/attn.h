@@ -369,9 +369,8 @@ int attn_set_bwd_pair(int enable);
  * Backward main kernel selection for later attn_bwd / attn_bwd_noalloc calls:
  * mode = 1 runs the persistent kernel (one CTA per SM taking the (head, key
  * tile) units in rounds), 0 the kernel with one CTA per unit, -1 (the
- * default; also ATTN_BWD_PERSIST at first use) chooses by size: persistent for
- * N <= 2048, and in atomic mode at every N without the causal mask and for
- * N <= 8192 with it.  Results meet the same
+ * default; also ATTN_BWD_PERSIST at first use) chooses: persistent in atomic
+ * mode at every N, and in deterministic mode for N <= 2048.  Results meet the same
  * tolerances either way; deterministic mode is bit-identical run to run with
  * either kernel (the two may differ from each other in the last bits).
  * Applies to d_qk = d_v = 64 and 128 without grouped-query heads or masks;

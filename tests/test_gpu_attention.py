@@ -381,6 +381,29 @@ def test_persistent_backward_many_units_per_cta(A):
         A.attn_set_bwd_persist(-1)
 
 
+@pytest.mark.parametrize("B,H,N", [(4, 16, 1024), (8, 16, 512)], ids=["key_tile_major", "head_major"])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_persistent_backward_atomic_unit_orders(A, B, H, N, causal):
+    """Atomic dQ on the persistent kernel with several rounds per CTA.  Under
+    the causal mask the units go key-tile-major over all heads when a round
+    holds at least two units of every head (64 heads here), head-major when
+    not (128 heads); first and last heads against the oracle."""
+    A.attn_set_bwd_persist(1)
+    try:
+        d = 128
+        t = G.inputs(B, H, N, d, d, seed=44)
+        o, lse = G.run_fwd(A, t, causal)
+        dq, dk, dv = G.run_bwd(A, t, o, lse, causal, 0)
+        G.check_status(A)
+        for b, h in ((0, 0), (B - 1, H - 1)):
+            q, k, v, do = (G.f64(t[n][b : b + 1, h : h + 1]) for n in ("q", "k", "v", "do"))
+            refs = ora.backward(q, k, v, do, 1.0 / math.sqrt(d), bool(causal))
+            for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+                G.assert_grad_close(name, G.f64(got[b : b + 1, h : h + 1]), ref)
+    finally:
+        A.attn_set_bwd_persist(-1)
+
+
 def test_deterministic_persistent_backward_on_two_unordered_streams(A):
     """Two deterministic persistent backward calls in flight at once on two
     streams with no ordering between them.  Each call's units wait on units of
