@@ -205,10 +205,17 @@ bool bwd_dims_ok(int d_qk, int d_v) {
 bool masked_dims_ok(int d_qk, int d_v) { return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128); }
 
 struct WorkspaceLayout {
-  size_t lse2, d, acc, tickets, total;
+  size_t lse2, d, acc, tickets, base;  // base: end of what every backward needs
+  size_t tail_part, total;  // the persistent kernel's cut units (atomic, d <= 128)
+  int tail_cap;             // pieces the tail region holds
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Pieces the persistent backward may cut its last round's units into: at most
+// one per CTA, and it runs one CTA per SM (152 on GB300), only when there are
+// more units than CTAs.
+constexpr int kMaxTailPieces = 160;
 
 WorkspaceLayout workspace_layout(int B, int H, int N, int d_qk, int deterministic) {
   WorkspaceLayout w;
@@ -219,7 +226,14 @@ WorkspaceLayout workspace_layout(int B, int H, int N, int d_qk, int deterministi
   w.d = round_up(w.lse2 + bh * npad * 4, 256);
   w.acc = round_up(w.d + bh * npad * 4, 256);
   w.tickets = round_up(w.acc + bh * npad * (size_t)d_qk * 4, 256);
-  w.total = round_up(w.tickets + (deterministic ? bh * tiles * 4 : 0), 256);
+  w.base = round_up(w.tickets + (deterministic ? bh * tiles * 4 : 0), 256);
+  // FP32 dV and dK partials of 128 rows x d per piece
+  const size_t units = bh * tiles;
+  w.tail_cap = (!deterministic && d_qk <= 128 && units > 1)
+                   ? (int)(units - 1 < (size_t)kMaxTailPieces ? units - 1 : (size_t)kMaxTailPieces)
+                   : 0;
+  w.tail_part = w.base;
+  w.total = round_up(w.tail_part + (size_t)w.tail_cap * 2 * 128 * d_qk * 4, 256);
   return w;
 }
 
@@ -655,7 +669,7 @@ namespace {
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
              void* dk, void* dv, int B, int H, int H_kv, int N, int d_qk, int d_v, int causal, float scale,
              int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-             const attn::MaskSpec* mask) {
+             const attn::MaskSpec* mask, bool tail_optional = false) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (H_kv < 1 || H_kv > H || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (int st = check_common(B, H, N, scale, causal)) return st;
@@ -665,7 +679,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return ATTN_ERR_MISALIGNED;
   const WorkspaceLayout w = workspace_layout(B, H, N, d_qk, deterministic);
-  if (workspace == nullptr || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
+  if (workspace == nullptr || workspace_bytes < (tail_optional ? w.base : w.total)) return ATTN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
   const Settings cfg = settings();
   attn::BwdParams p;
@@ -732,6 +746,10 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   p.row_d = reinterpret_cast<float*>(ws + w.d);
   p.dq_acc = reinterpret_cast<float*>(ws + w.acc);
   p.tickets = deterministic ? reinterpret_cast<int*>(ws + w.tickets) : nullptr;
+  if (w.tail_cap > 0 && workspace_bytes >= w.total) {
+    p.tail_part = reinterpret_cast<float*>(ws + w.tail_part);
+    p.tail_cap = w.tail_cap;
+  }
   p.timeout_ns = cfg.timeout_ns;
   p.N = N;
   p.n_tiles = (N + 127) / 128;
@@ -771,6 +789,20 @@ int make_mask(attn::MaskSpec* m, int N, int window_left, int window_right, const
 }
 
 }  // namespace
+
+namespace attn {
+
+// attn_bwd_noalloc's backward: attn_bwd on the library's fixed scratch array,
+// which may be too small for the region of the persistent kernel's cut units
+// only (its last round then runs whole units).
+int bwd_on_scratch(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale,
+                   int deterministic, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d_qk, d_v, causal, scale, deterministic, scratch,
+                  scratch_bytes, stream, nullptr, true);
+}
+
+}  // namespace attn
 
 extern "C" {
 

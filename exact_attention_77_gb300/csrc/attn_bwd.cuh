@@ -28,7 +28,9 @@
 //                    reduce-add copies from a shared-memory staging tile
 //                    (atomic mode), or with the same copies in ascending-j
 //                    order behind a per-(b, h, i) ticket (deterministic mode).
-//   dq_convert_kernel  dQ = scale * accumulator, as bf16 [B,H,N,d].
+//   dq_convert_kernel  dQ = scale * accumulator, as bf16 [B,H,N,d]; and the
+//                    dV / dK rows of units the persistent kernel cut into
+//                    pieces: the pieces' FP32 partials summed in piece order.
 //
 // Warp roles in bwd_kernel (512 threads): warp 0 producer (TMA), warp 1 MMA
 // issuer and tensor-memory owner, warps 4-7 and 8-11 two compute warpgroups
@@ -194,10 +196,59 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdParams p) {
 // groups; a warp takes 32 consecutive rows of the same groups, so each of
 // its loads reads 512 contiguous bytes and each thread writes 32 contiguous
 // bytes of its dQ row (one whole sector).
+// Blocks past the dQ ones (dq_convert_blocks) finish the units the
+// persistent kernel cut: one thread per (unit, tensor, key row, 8 columns),
+// a warp on two rows of one tensor, reading the pieces' FP32 partials (slots
+// of consecutive CTAs) and writing 16 bytes of bf16.  Those units are
+// head-major like the persistent kernel's (unit u: head u / n_tiles, key tile
+// u mod n_tiles).
+template <int D>
+__host__ __device__ __forceinline__ long dq_convert_blocks(const BwdParams& p) {
+  return ((long)p.BH * p.n_tiles * 128 * (D / 16) + 255) / 256;
+}
+
+template <int D>
+inline long tail_sum_blocks(const BwdParams& p) {
+  return p.tail_s > 1 ? ((long)p.tail_units * 2 * 128 * (D / 8) + 255) / 256 : 0;
+}
+
+template <int D>
+__device__ __forceinline__ void tail_sum(const BwdParams& p, long y) {
+  constexpr int kChunks = D / 8;
+  if (y >= (long)p.tail_units * 2 * 128 * kChunks) return;
+  const int c8 = (int)(y % kChunks);
+  const int row = (int)((y / kChunks) % 128);
+  const int pass = (int)((y / (kChunks * 128)) % 2);  // 0: dV, 1: dK
+  const int q = (int)(y / (kChunks * 128 * 2));       // cut unit
+  const int u = p.tail_first + q;
+  const int bh = u / p.n_tiles, j = u - bh * p.n_tiles;
+  const int k_glob = j * 128 + row;
+  if (k_glob >= p.N) return;
+  constexpr size_t kSlot = 2 * (size_t)128 * D;
+  const float* src = p.tail_part + (size_t)q * p.tail_s * kSlot + (size_t)(pass * 128 + row) * D + c8 * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int k = 0; k < p.tail_s; ++k) {
+    const float4 a = *reinterpret_cast<const float4*>(src + (size_t)k * kSlot);
+    const float4 b = *reinterpret_cast<const float4*>(src + (size_t)k * kSlot + 4);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  }
+  const float mul = pass == 0 ? 1.f : p.scale;
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pass == 0 ? p.dv : p.dk) +
+                                        ((size_t)bh * p.N + k_glob) * D + c8 * 8);
+  *dst = make_uint4(pack_bf16(acc[0] * mul, acc[1] * mul), pack_bf16(acc[2] * mul, acc[3] * mul),
+                    pack_bf16(acc[4] * mul, acc[5] * mul), pack_bf16(acc[6] * mul, acc[7] * mul));
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) dq_convert_kernel(BwdParams p) {
   constexpr int kGroups = D / 4;    // 32 or 16
   constexpr int kQuads = kGroups / 4;  // threads per row
+  const long nb = dq_convert_blocks<D>(p);
+  if ((long)blockIdx.x >= nb) {
+    tail_sum<D>(p, ((long)blockIdx.x - nb) * blockDim.x + threadIdx.x);
+    return;
+  }
   const long x = (long)blockIdx.x * blockDim.x + threadIdx.x;
   const long per_tile = 128L * kQuads;
   const long tile_g = x / per_tile;  // over BH * n_tiles
@@ -871,7 +922,7 @@ cudaError_t launch_bwd2_main(const BwdParams& p, cudaStream_t stream);
 
 // Persistent main kernel for short sequences (attn_bwd_persist.cuh).
 template <int D, bool CAUSAL, bool DET>
-cudaError_t launch_bwd_persist_main(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_persist_main(BwdParams& p, cudaStream_t stream);
 
 template <int D, bool CAUSAL, bool DET, bool MASK = false, bool GQA = false>
 cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const LaunchEvents* evs) {
@@ -898,9 +949,11 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
       paired = true;
     }
   }
+  BwdParams pc = p;  // the persistent launch adds its cut-tail plan, which the conversion finishes
+  pc.tail_s = 1;
   if constexpr (!MASK && !GQA) {
     if (!paired && p.persist) {
-      cudaError_t e = launch_bwd_persist_main<D, CAUSAL, DET>(p, stream);
+      cudaError_t e = launch_bwd_persist_main<D, CAUSAL, DET>(pc, stream);
       if (e != cudaSuccess) return e;
       paired = true;  // (the main kernel has run: skip the one-unit launch)
     }
@@ -918,9 +971,8 @@ cudaError_t launch_bwd_instance(const BwdParams& p, cudaStream_t stream, const L
   }
   mark(2);
   {
-    const long threads = (long)p.BH * p.n_tiles * 128 * (D / 16);
-    const long blocks = (threads + 255) / 256;
-    dq_convert_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    const long blocks = dq_convert_blocks<D>(pc) + tail_sum_blocks<D>(pc);
+    dq_convert_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(pc);
     cudaError_t e = cudaGetLastError();
     mark(3);
     return e;

@@ -58,19 +58,42 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
   // units to the shortest, and a head's units in a round share its Q / dO
   // reads in L2); head-major otherwise (resident CTAs share one or two
   // heads' Q, dO and dQ accumulators in L2).  Causal key tiles with small j
-  // are the longest and go first in either order.  GQA: walk position qi = g * n + i over query head g of the group
-  // and query tile i (from n-1 down to i_lo, head after head); the first
-  // query head of K/V head bh is qh0.  Deterministic and non-causal: the
+  // are the longest and go first in either order.  GQA: walk position
+  // qi = g * n + i over query head g of the group and query tile i (from n-1
+  // down to i_lo, head after head); the first query head of K/V head bh is
+  // qh0.  Deterministic and non-causal: the
   // rotated walk of det_order.h (every CTA is resident, the kernel being
   // launched cooperatively), unit jj starting at query tile
   // (n - 1 - sigma jj) mod n and wrapping from 0 to n - 1.
   constexpr bool kRot = DETERMINISTIC && !CAUSAL && !MASK && !GQA;
   const bool causal_ktm = 2 * n_heads <= (int)gridDim.x;
+  // persistent CTAs take unit r G + b in round r (G - 1 - b on odd rounds, so
+  // that with the longest units first every CTA gets a similar total); each
+  // CTA's units increase from round to round.
+  // Cut tail (atomic dQ, no causal mask; the units are all equal): when the
+  // last round is partial, rem units for G CTAs, every CTA but rem would idle
+  // for a whole unit.  Instead its units are cut into s = min(G / rem, n)
+  // pieces of contiguous query tiles, one per CTA (CTA b takes piece b mod s
+  // of tail unit b / s), and the round takes about 1/s of a unit.  Each piece
+  // leaves FP32 dV / dK partials in slot b of p.tail_part, and the dQ
+  // conversion that follows the kernel sums each unit's slots in piece order
+  // into dV and dK.  (Measured on GB300, d = 128, H = 16: 2048 units are
+  // 13.47 rounds and ran at 1316 TFLOP/s against ~1360 for unit counts that
+  // fill their last round.)
+  constexpr bool kTail = !DETERMINISTIC && !CAUSAL && !MASK && !GQA;
+  const int n_units = PERSIST ? n_heads * n : (int)gridDim.x;
+  const int G = gridDim.x;
+  const int n_rounds = PERSIST ? (n_units + G - 1) / G : 1;
+  const int n_full = n_units / G;
+  const int rem = n_units - n_full * G;
+  const int tail_s = (kTail && PERSIST && p.tail_s > 1) ? p.tail_s : 1;  // the launch's plan
   struct BUnit {
     int j, bh, i_lo, n_it, qh0, i_first;
+    int piece;  // piece of a cut unit (-1: the whole unit)
   };
-  auto unit_at = [&](int u) {
+  auto unit_at = [&](int u, int piece) {
     BUnit w;
+    w.piece = piece;
     if (DETERMINISTIC) {
       det_unit(u, n_heads, n, p.det_group, p.det_desc, w.j, w.bh);
     } else if (CAUSAL && causal_ktm) {
@@ -97,6 +120,11 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       const DetRot d = det_rot(u, (int)gridDim.x, n_heads, n, p.det_group, p.det_desc);
       w.i_first = det_rot_first(d.jj, n, d.sigma);
     }
+    if (kTail && piece >= 0) {  // query tiles [lo, hi), from hi - 1 down
+      const int lo = piece * n / tail_s, hi = (piece + 1) * n / tail_s;
+      w.i_first = hi - 1;
+      w.n_it = hi - lo;
+    }
     return w;
   };
   auto tile_i = [&](int qi) { return GQA ? qi % n : qi; };
@@ -106,14 +134,16 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
     if (kRot) return i > 0 ? i - 1 : n - 1;
     return MASK ? mask_prev_query_tile(p.mask, w.j, i) : i - 1;
   };
-  // persistent CTAs take unit r G + b in round r (G - 1 - b on odd rounds, so
-  // that with the longest units first every CTA gets a similar total); each
-  // CTA's units increase from round to round
-  const int n_units = PERSIST ? n_heads * n : (int)gridDim.x;
-  const int G = gridDim.x;
-  const int n_rounds = PERSIST ? (n_units + G - 1) / G : 1;
-  auto unit_of_round = [&](int rd) {
-    return PERSIST ? rd * G + ((rd & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x) : (int)blockIdx.x;
+  // the unit (n_units: none) and piece (-1: whole) of this CTA's round rd
+  auto unit_of_round = [&](int rd, int& piece) {
+    const int b = (int)blockIdx.x;
+    piece = -1;
+    if (!PERSIST) return b;
+    if (kTail && tail_s > 1 && rd == n_full) {
+      piece = b % tail_s;
+      return b < rem * tail_s ? n_full * G + b / tail_s : n_units;
+    }
+    return rd * G + ((rd & 1) ? G - 1 - b : b);
   };
 
   if (threadIdx.x == 0) {
@@ -151,9 +181,10 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       int t = 0, ucnt = 0;              // tiles and units started
       bool ok = true;
       for (int rd = 0; ok && rd < n_rounds; ++rd) {
-        const int u = unit_of_round(rd);
+        int pc;
+        const int u = unit_of_round(rd, pc);
         if (PERSIST && u >= n_units) continue;
-        const BUnit w = unit_at(u);
+        const BUnit w = unit_at(u, pc);
         // K and V of the previous unit are read until its last products complete
         if (PERSIST && ucnt > 0 && !(ok = mbar_wait(bar(L::kBarKVEmpty), (ucnt - 1) & 1, ctl, kBWhereProd + 2)))
           break;
@@ -238,9 +269,10 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       bool ok = true;
       int t = 0, ucnt = 0;  // tiles and units done
       for (int rd = 0; ok && rd < n_rounds; ++rd) {
-      const int u = unit_of_round(rd);
+      int pc;
+      const int u = unit_of_round(rd, pc);
       if (PERSIST && u >= n_units) continue;
-      const BUnit w = unit_at(u);
+      const BUnit w = unit_at(u, pc);
       if (!(ok = mbar_wait(bar(L::kBarKV), ucnt & 1, ctl, kBWhereMma))) break;
       tc_fence_after();
       for (int it = 0; ok && it < w.n_it; ++it) {
@@ -325,9 +357,10 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
       bool ok = true;
       int t = 0;  // tiles of earlier units
       for (int rd = 0; ok && rd < n_rounds; ++rd) {
-        const int u = unit_of_round(rd);
+        int pc;
+        const int u = unit_of_round(rd, pc);
         if (PERSIST && u >= n_units) continue;
-        const BUnit w = unit_at(u);
+        const BUnit w = unit_at(u, pc);
         const int j = w.j;
         const DetRot dr = kRot ? det_rot(u, (int)gridDim.x, n_heads, n, p.det_group, p.det_desc) : DetRot{};
         for (int it = 0, qi = w.i_first; ok && it < w.n_it; ++it, qi = i_next(w, qi)) {
@@ -391,7 +424,9 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
           if (mbar_test(b, par)) return;
         live = false;
       };
-      const int n_it0 = unit_of_round(0) < n_units ? unit_at(unit_of_round(0)).n_it : 0;  // the first unit only
+      int pc0;
+      const int u0 = unit_of_round(0, pc0);
+      const int n_it0 = u0 < n_units ? unit_at(u0, pc0).n_it : 0;  // the first unit only
       for (int it = 0; live && it < n_it0 && it < kTraceIters; ++it) {
         seen(bar(L::kBarSFull), it & 1);
         ATTN_TRACE_AT(blockIdx.x, it, 16);
@@ -427,9 +462,10 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
     bool ok = true;
     int t = 0, ucnt = 0;  // tiles and units done
     for (int rd = 0; ok && rd < n_rounds; ++rd) {
-    const int u = unit_of_round(rd);
+    int pc;
+    const int u = unit_of_round(rd, pc);
     if (PERSIST && u >= n_units) continue;
-    const BUnit w = unit_at(u);
+    const BUnit w = unit_at(u, pc);
     const int j = w.j;
     const int k_glob = j * kBTile + lrow;
     const bool key_dead = k_glob >= p.N;
@@ -548,7 +584,10 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), ucnt & 1, ctl, kBWhereFin));
     {
       ok = named_bar_and(2, 256, ok);  // both compute warpgroups (the stores below need every row)
-      if (ok) {
+      // (a piece of a cut unit is always the CTA's last: its epilogue follows
+      // the loop, so that none of its addresses stay live through the tiles)
+      if (kTail && w.piece >= 0) {
+      } else if (ok) {
         tc_fence_after();
         constexpr int kBoxes = D / 64;
         constexpr uint32_t kBoxBytes = kBTile * 128;
@@ -590,6 +629,26 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
     t += w.n_it;
     ++ucnt;
     }  // units
+    if (kTail && ok && tail_s > 1) {
+      // a piece of a cut unit (its accumulators complete, waited for above):
+      // this thread's FP32 dV / dK partials, its key row and its warpgroup's
+      // half of the columns, into the CTA's slot
+      int pc;
+      if (unit_of_round(n_full, pc) < n_units) {
+        tc_fence_after();
+        float* mine = p.tail_part + (size_t)blockIdx.x * (2 * kBTile * D);
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+          for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+            float a[32];
+            tmem_ld32(tmem + lane_base + (pass == 0 ? L::kColDV : L::kColDK) + c0, a);
+            float4* dst = reinterpret_cast<float4*>(mine + (size_t)(pass * kBTile + lrow) * D + c0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) dst[v] = make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+          }
+      }
+    }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kDqRegs));
     // ========================== dQ warpgroup ===========================
@@ -604,9 +663,10 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
     bool ok = true;
     int t = 0;  // tiles done
     for (int rd = 0; ok && rd < n_rounds; ++rd) {
-    const int u = unit_of_round(rd);
+    int pc;
+    const int u = unit_of_round(rd, pc);
     if (PERSIST && u >= n_units) continue;
-    const BUnit w = unit_at(u);
+    const BUnit w = unit_at(u, pc);
     const int j = w.j;
     for (int it = 0, qi = w.i_first; it < w.n_it; ++it, qi = i_next(w, qi)) {
       const int tt = t + it;
@@ -707,7 +767,7 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
 }
 
 template <int D, bool CAUSAL, bool DET>
-cudaError_t launch_bwd_persist_main(const BwdParams& p, cudaStream_t stream) {
+cudaError_t launch_bwd_persist_main(BwdParams& p, cudaStream_t stream) {
   using L = BwdPLayout<D>;
   auto kernel = bwd_persist_kernel<D, CAUSAL, DET>;
   int sms = 0;
@@ -715,6 +775,23 @@ cudaError_t launch_bwd_persist_main(const BwdParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int n_units = p.BH * p.n_tiles;
   const int grid = n_units < sms ? n_units : sms;  // one CTA per SM
+  // the cut tail (atomic dQ without the causal mask; see the kernel): the
+  // last round's rem units in s = min(grid / rem, n_tiles) pieces, as many as
+  // the workspace has slots for
+  p.tail_s = 1;
+  if (!DET && !CAUSAL && p.tail_part != nullptr) {
+    const int n_full = n_units / grid, rem = n_units - n_full * grid;
+    if (n_full > 0 && rem > 0) {
+      int s = grid / rem;
+      if (s > p.n_tiles) s = p.n_tiles;
+      if (s * rem > p.tail_cap) s = p.tail_cap / rem;
+      if (s > 1) {
+        p.tail_s = s;
+        p.tail_first = n_full * grid;
+        p.tail_units = rem;
+      }
+    }
+  }
   if constexpr (DET) {
     // Deterministic mode: a unit's dQ additions wait for lower-numbered units,
     // which on later rounds belong to other CTAs (some with a higher index),

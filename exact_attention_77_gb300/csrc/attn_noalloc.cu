@@ -49,16 +49,23 @@ int noalloc_scratch(void** out) {
 
 }  // namespace
 
+namespace attn {
+int bwd_on_scratch(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d_qk, int d_v, int causal, float scale,
+                   int deterministic, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+}  // namespace attn
+
 extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d_qk,
                                 int d_v, int causal, float scale, int deterministic, cudaStream_t stream) {
   const size_t need = attn_bwd_workspace_bytes(B, H, N, d_qk, d_v, deterministic);
-  // need == 0: sizes the backward rejects; attn_bwd reports the exact error
-  if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
+  // need == 0: sizes the backward rejects, which it reports with the exact
+  // error; a workspace larger than the array is an error unless all that does
+  // not fit is the optional region for the persistent kernel's cut units
   void* scratch = nullptr;
   if (need != 0) {
     if (int st = noalloc_scratch(&scratch)) return st;
   }
-  return attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, causal, scale, deterministic, scratch,
-                  need != 0 ? (size_t)ATTN_NOALLOC_SCRATCH_BYTES : 0, stream);
+  return attn::bwd_on_scratch(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d_qk, d_v, causal, scale, deterministic,
+                              scratch, need != 0 ? (size_t)ATTN_NOALLOC_SCRATCH_BYTES : 0, stream);
 }

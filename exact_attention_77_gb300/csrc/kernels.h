@@ -105,6 +105,17 @@ struct BwdParams {
   // contribution (ticket 0) is a plain bulk store, so the preprocess leaves
   // the FP32 accumulator unzeroed
   int acc_first_store;
+  // atomic dQ, persistent kernel without the causal mask: when its last round
+  // is partial, that round's tail_units units (from unit tail_first on) are
+  // cut into tail_s pieces over the query tiles, one per CTA; the piece of CTA
+  // b leaves FP32 dV / dK partials in slot b ([slot][2][128][d], dV then dK),
+  // which the dQ conversion sums into dV and dK.  tail_cap slots fit (0: units
+  // are never cut); tail_s <= 1: no cut (set by the persistent launch).
+  float* tail_part;
+  int tail_cap;
+  int tail_s;
+  int tail_first;
+  int tail_units;
 };
 
 // Optional events recorded on the launch stream around each backward kernel:

@@ -89,7 +89,10 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* ls
  * backward does not accept).  The workspace holds, per (b, h): the FP32 row
  * terms D_i = dO_i . O_i and LSE_i * log2(e) (padded to a multiple of 128
  * rows), the FP32 dQ accumulator, and (deterministic mode) one int32 ticket per
- * 128-row query tile.
+ * 128-row query tile.  With atomic dQ at d_qk = d_v = 64 or 128 it also holds
+ * the region where the persistent backward kernel leaves the pieces of the
+ * units it cuts in its last round: FP32 dV and dK partials of 128 rows per
+ * piece, for min(160, B*H*ceil(N/128) - 1) pieces.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d_qk, int d_v, int deterministic);
 
@@ -484,8 +487,11 @@ int attn_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
  * ATTN_NOALLOC_SCRATCH_BYTES inside the library; nothing is allocated.
  *   Arguments, layouts and results are those of attn_bwd without
  *   ``workspace`` / ``workspace_bytes``.
- *   Sizes whose attn_bwd_workspace_bytes exceeds ATTN_NOALLOC_SCRATCH_BYTES
- *   return ATTN_ERR_WORKSPACE; other argument errors as attn_bwd.
+ *   Sizes whose workspace does not fit ATTN_NOALLOC_SCRATCH_BYTES return
+ *   ATTN_ERR_WORKSPACE, other argument errors as attn_bwd.  When only the
+ *   persistent kernel's region for cut units (see attn_bwd_workspace_bytes)
+ *   does not fit, the call runs without it: that kernel's last round then
+ *   takes whole units.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
  *   before any stream capture.

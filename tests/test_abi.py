@@ -64,8 +64,15 @@ def test_workspace_sizes(lib):
     b, h, n, d = 1, 2, 300, 64
     npad = 384
     base = 2 * b * h * npad * 4 + b * h * npad * d * 4
-    assert lib.attn_bwd_workspace_bytes(b, h, n, d, d, 0) == base
+    # atomic mode at d <= 128 adds the persistent kernel's region for the
+    # pieces of cut units: FP32 dV + dK, 128 rows each, for min(160, units - 1)
+    # pieces
+    pieces = min(160, b * h * 3 - 1)
+    assert lib.attn_bwd_workspace_bytes(b, h, n, d, d, 0) == base + pieces * 2 * 128 * d * 4
     assert lib.attn_bwd_workspace_bytes(b, h, n, d, d, 1) == base + 256
+    assert lib.attn_bwd_workspace_bytes(1, 1, 100, d, d, 0) == 2 * 128 * 4 + 128 * d * 4  # one unit: never cut
+    assert lib.attn_bwd_workspace_bytes(4, 16, 1024, 128, 128, 0) == (
+        2 * 64 * 1024 * 4 + 64 * 1024 * 128 * 4 + 160 * 2 * 128 * 128 * 4)
     # d_qk = 192: the accumulator is d_qk wide
     assert lib.attn_bwd_workspace_bytes(1, 1, 128, 192, 128, 0) == 2 * 128 * 4 + 128 * 192 * 4
     assert lib.attn_bwd_workspace_bytes(1, 1, 128, 192, 192, 0) == 0
@@ -108,9 +115,10 @@ def test_backward_argument_errors(lib):
     assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 3, p, ok_ws, None) == A.ATTN_ERR_INVALID_ARG
     assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 0, None, ok_ws, None) == A.ATTN_ERR_WORKSPACE
     assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 0, p, ok_ws - 1, None) == A.ATTN_ERR_WORKSPACE
+    # deterministic mode: tickets, and no region for cut units (atomic only)
     det_ws = lib.attn_bwd_workspace_bytes(1, 2, 256, 64, 64, 1)
-    assert det_ws > ok_ws
-    assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 1, p, ok_ws, None) == A.ATTN_ERR_WORKSPACE
+    assert det_ws != ok_ws
+    assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 1, p, det_ws - 1, None) == A.ATTN_ERR_WORKSPACE
     assert f(p, p, p, p, p, p, p, 0x1002, p, 1, 2, 256, 64, 64, 0, 0.1, 0, p, ok_ws, None) == A.ATTN_ERR_MISALIGNED
     assert f(p, p, p, p, p, p, p, p, p, 1, 2, 256, 64, 64, 0, 0.1, 0, 0x1004, ok_ws, None) == A.ATTN_ERR_MISALIGNED
 

@@ -404,6 +404,45 @@ def test_persistent_backward_atomic_unit_orders(A, B, H, N, causal):
         A.attn_set_bwd_persist(-1)
 
 
+@pytest.mark.parametrize(
+    "B,H,N",
+    [(1, 20, 1024), (1, 17, 1152), (1, 16, 2560), (1, 20, 1000), (4, 16, 1024)],
+    ids=["8_pieces_of_one_tile", "rem_1_9_pieces", "9_ragged_pieces", "ragged_keys", "2_pieces"],
+)
+def test_persistent_backward_cut_last_round(A, B, H, N):
+    """Atomic dQ without the causal mask: more units than CTAs, the last round
+    partial, so its units are cut into pieces over the query tiles whose FP32
+    dV / dK partials the conversion kernel sums.  The last head (its units in the
+    cut round) and the first (whole units) against the oracle; every head
+    against the one-CTA-per-unit kernel."""
+    torch = G.torch_mod()
+    d = 128
+    t = G.inputs(B, H, N, d, d, seed=45)
+    o, lse = G.run_fwd(A, t, 0)
+    A.attn_set_bwd_persist(1)
+    try:
+        got = G.run_bwd(A, t, o, lse, 0, 0)
+        G.check_status(A)
+        again = G.run_bwd(A, t, o, lse, 0, 0)
+        G.check_status(A)
+    finally:
+        A.attn_set_bwd_persist(0)
+    try:
+        one = G.run_bwd(A, t, o, lse, 0, 0)
+        G.check_status(A)
+    finally:
+        A.attn_set_bwd_persist(-1)
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        q, k, v, do = (G.f64(t[n][b : b + 1, h : h + 1]) for n in ("q", "k", "v", "do"))
+        refs = ora.backward(q, k, v, do, 1.0 / math.sqrt(d), False)
+        for name, x, ref in zip(("dq", "dk", "dv"), got, refs):
+            G.assert_grad_close(name, G.f64(x[b : b + 1, h : h + 1]), ref)
+    for name, x, y, z in zip(("dq", "dk", "dv"), got, one, again):
+        G.assert_grad_close(name, G.f64(x), G.f64(y))
+        if name != "dq":  # dK / dV: the pieces are summed in a fixed order
+            assert torch.equal(x.view(torch.int16), z.view(torch.int16)), name
+
+
 def test_deterministic_persistent_backward_on_two_unordered_streams(A):
     """Two deterministic persistent backward calls in flight at once on two
     streams with no ordering between them.  Each call's units wait on units of

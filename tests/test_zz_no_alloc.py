@@ -50,6 +50,24 @@ def test_noalloc_matches_workspace_backward_twice(A, causal, det):
                 assert torch.equal(got.view(torch.int16), want.view(torch.int16)), name
 
 
+def test_noalloc_without_the_cut_unit_region(A):
+    # 352 units: the persistent kernel would cut its last round, but only the
+    # workspace without the region for the pieces fits the array
+    B, H, N, d = 1, 11, 4096, 128
+    base = 2 * B * H * N * 4 + B * H * N * d * 4
+    assert base <= A.ATTN_NOALLOC_SCRATCH_BYTES < A.attn_bwd_workspace_bytes(B, H, N, d, d, 0)
+    torch = G.torch_mod()
+    t = G.inputs(B, H, N, d, d, seed=18)
+    o, lse = G.run_fwd(A, t, 0)
+    ref = G.run_bwd(A, t, o, lse, 0, 0)
+    out = [torch.full_like(x, float("nan")) for x in ref]
+    A.attn_bwd_noalloc(t["q"], t["k"], t["v"], o, t["do"], lse, out[0], out[1], out[2], B, H, N, d, d, 0,
+                       1.0 / math.sqrt(d), 0)
+    G.check_status(A)
+    for name, got, want in zip(("dq", "dk", "dv"), out, ref):
+        G.assert_grad_close(name, G.f64(got), G.f64(want))
+
+
 def test_noalloc_rejects_sizes_beyond_its_array(A):
     # 16 heads x 16384 rows x 128 dims of FP32 accumulator alone is 128 MiB
     p = 0x1000
