@@ -384,6 +384,18 @@ def run_ours(args, world, rank, local):
     while BH % n_chunks:
         n_chunks -= 1
     hc = BH // n_chunks
+    # groups as (first head, heads); with --e2e-taper the first and last
+    # groups are halved, so the pipeline fills (the first group's inputs
+    # going up before any kernel runs) and drains (the last group's results
+    # coming down after the last kernel) with half as many bytes
+    sizes = [hc] * n_chunks
+    if args.e2e_taper and hc >= 2 and n_chunks >= 2:
+        sizes = [hc // 2, hc - hc // 2] + [hc] * (n_chunks - 2) + [hc - hc // 2, hc // 2]
+    groups, h0 = [], 0
+    for sz in sizes:
+        groups.append((h0, sz))
+        h0 += sz
+    n_chunks = len(groups)
     flat = lambda x: x.reshape(BH, *x.shape[2:])
     pairs_in = [(flat(dst), flat(src)) for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo))]
     pairs_out = [(flat(dst), flat(src)) for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv))]
@@ -404,8 +416,8 @@ def run_ours(args, world, rank, local):
         s_out.wait_event(ev_start)
         for cs in s_comp[1:]:
             cs.wait_event(ev_start)
-        for c in range(n_chunks):
-            sl = slice(c * hc, (c + 1) * hc)
+        for c, (g0, gn) in enumerate(groups):
+            sl = slice(g0, g0 + gn)
             cs = s_comp[c % n_cs]
             if not first[0]:
                 s_in.wait_event(ev_done[c])  # the previous step's group c no longer reads these inputs
@@ -417,8 +429,8 @@ def run_ours(args, world, rank, local):
             if not first[0]:
                 cs.wait_event(ev_out[c])  # the previous step's results of group c are out
             cq, ck, cv, co, cdo, clse, cdq, cdk, cdv = (x[sl] for x in dev_t)
-            A.attn_fwd(cq, ck, cv, co, clse, 1, hc, N, d, dvh, args.causal, scale, cs)
-            A.attn_bwd(cq, ck, cv, co, cdo, clse, cdq, cdk, cdv, 1, hc, N, d, dvh, args.causal, scale, args.det,
+            A.attn_fwd(cq, ck, cv, co, clse, 1, gn, N, d, dvh, args.causal, scale, cs)
+            A.attn_bwd(cq, ck, cv, co, cdo, clse, cdq, cdk, cdv, 1, gn, N, d, dvh, args.causal, scale, args.det,
                        cwsb[c % n_cs], cws, cs)
             ev_done[c].record(cs)
             s_out.wait_event(ev_done[c])
@@ -484,7 +496,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk, "gpu_launches": launches, "sustained": sustained,
         "e2e": {"value": world * f_step / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "head_groups": n_chunks,
-                "compute_streams": n_cs},
+                "group_heads": sizes, "compute_streams": n_cs},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
@@ -818,6 +830,8 @@ def main(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="head groups pipelined through host copies and compute in the e2e leg")
     ap.add_argument("--e2e-streams", type=int, default=3, help="compute streams the e2e leg deals its groups to")
+    ap.add_argument("--e2e-taper", type=int, default=1, choices=(0, 1),
+                    help="1: halve the e2e leg's first and last head groups (shorter pipeline fill and drain)")
     ap.add_argument("--case", choices=("step", "fp8", "splitkv", "masked", "exp2", "detsched", "sweep"), default="step",
                     help="step: the benchmark contract; others time the library's other paths")
     ap.add_argument("--Nq", type=int, default=1)
