@@ -397,8 +397,12 @@ def run_ours(args, world, rank, local):
         h0 += sz
     n_chunks = len(groups)
     flat = lambda x: x.reshape(BH, *x.shape[2:])
-    pairs_in = [(flat(dst), flat(src)) for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo))]
-    pairs_out = [(flat(dst), flat(src)) for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv))]
+    # the forward needs Q, K, V only, and O / LSE are final once it has run:
+    # dO goes up after them and O / LSE come down before the gradients
+    pairs_fwd_in = [(flat(dst), flat(src)) for dst, src in ((q, hq), (k, hk), (v, hv))]
+    pairs_bwd_in = [(flat(do), flat(hdo))]
+    pairs_fwd_out = [(flat(dst), flat(src)) for dst, src in ((ho, o), (hlse, lse))]
+    pairs_bwd_out = [(flat(dst), flat(src)) for dst, src in ((hdq, dq), (hdk, dk), (hdv, dv))]
     dev_t = [flat(x) for x in (q, k, v, o, do, lse, dq, dk, dv)]
     cws = A.attn_bwd_workspace_bytes(1, hc, N, d, dvh, args.det)
     n_cs = max(1, min(args.e2e_streams, n_chunks))  # compute streams, groups dealt round-robin
@@ -407,6 +411,7 @@ def run_ours(args, world, rank, local):
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
     ev_in, ev_done, ev_out = [ev() for _ in range(n_chunks)], [ev() for _ in range(n_chunks)], [ev() for _ in range(n_chunks)]
+    ev_fin, ev_fdone = [ev() for _ in range(n_chunks)], [ev() for _ in range(n_chunks)]
     ev_start = ev()
     first = [True]
 
@@ -422,20 +427,29 @@ def run_ours(args, world, rank, local):
             if not first[0]:
                 s_in.wait_event(ev_done[c])  # the previous step's group c no longer reads these inputs
             with torch.cuda.stream(s_in):
-                for dst, src in pairs_in:
+                for dst, src in pairs_fwd_in:
+                    dst[sl].copy_(src[sl], non_blocking=True)
+                ev_fin[c].record(s_in)
+                for dst, src in pairs_bwd_in:
                     dst[sl].copy_(src[sl], non_blocking=True)
             ev_in[c].record(s_in)
-            cs.wait_event(ev_in[c])
+            cs.wait_event(ev_fin[c])
             if not first[0]:
                 cs.wait_event(ev_out[c])  # the previous step's results of group c are out
             cq, ck, cv, co, cdo, clse, cdq, cdk, cdv = (x[sl] for x in dev_t)
             A.attn_fwd(cq, ck, cv, co, clse, 1, gn, N, d, dvh, args.causal, scale, cs)
+            ev_fdone[c].record(cs)
+            cs.wait_event(ev_in[c])
             A.attn_bwd(cq, ck, cv, co, cdo, clse, cdq, cdk, cdv, 1, gn, N, d, dvh, args.causal, scale, args.det,
                        cwsb[c % n_cs], cws, cs)
             ev_done[c].record(cs)
+            s_out.wait_event(ev_fdone[c])
+            with torch.cuda.stream(s_out):
+                for dst, src in pairs_fwd_out:
+                    dst[sl].copy_(src[sl], non_blocking=True)
             s_out.wait_event(ev_done[c])
             with torch.cuda.stream(s_out):
-                for dst, src in pairs_out:
+                for dst, src in pairs_bwd_out:
                     dst[sl].copy_(src[sl], non_blocking=True)
             ev_out[c].record(s_out)
         first[0] = False
