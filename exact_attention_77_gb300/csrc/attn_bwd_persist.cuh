@@ -53,18 +53,18 @@ __global__ void __launch_bounds__(512, 1) bwd_persist_kernel(const __grid_consta
   const int n_heads = GQA ? p.BH / p.kv_group : p.BH;  // K/V heads
   // work unit u: key tile j of K/V head bh.  Key-tile-major in groups of
   // heads in deterministic mode (a unit waits only on units ordered before
-  // it) and under the causal mask when a round of G units holds two or more
-  // units of every head (G >= 2 heads: the rounds then go from the longest
-  // units to the shortest, and a head's units in a round share its Q / dO
-  // reads in L2); head-major otherwise (resident CTAs share one or two
-  // heads' Q, dO and dQ accumulators in L2).  Causal key tiles with small j
-  // are the longest and go first in either order.  GQA: walk position
-  // qi = g * n + i over query head g of the group and query tile i (from n-1
-  // down to i_lo, head after head); the first query head of K/V head bh is
-  // qh0.  Deterministic and non-causal: the
-  // rotated walk of det_order.h (every CTA is resident, the kernel being
-  // launched cooperatively), unit jj starting at query tile
-  // (n - 1 - sigma jj) mod n and wrapping from 0 to n - 1.
+  // it), and over all heads under the causal mask when a round of G units
+  // holds two or more units of every head (2 x heads <= G: the rounds then
+  // go from the longest units to the shortest, and a head's units in a
+  // round share its Q / dO reads in L2); head-major otherwise (resident
+  // CTAs share one or two heads' Q, dO and dQ accumulators in L2).  Causal
+  // key tiles with small j are the longest and go first in either order.
+  // GQA: walk position qi = g * n + i over query head g of the group and
+  // query tile i (from n-1 down to i_lo, head after head); the first query
+  // head of K/V head bh is qh0.  Deterministic and non-causal: the rotated
+  // walk of det_order.h (every CTA is resident, the kernel being launched
+  // cooperatively), unit jj starting at query tile (n - 1 - sigma jj) mod n
+  // and wrapping from 0 to n - 1.
   constexpr bool kRot = DETERMINISTIC && !CAUSAL && !MASK && !GQA;
   const bool causal_ktm = 2 * n_heads <= (int)gridDim.x;
   // persistent CTAs take unit r G + b in round r (G - 1 - b on odd rounds, so

@@ -482,6 +482,47 @@ def test_deterministic_persistent_backward_on_two_unordered_streams(A):
         A.attn_set_bwd_persist(-1)
 
 
+def test_atomic_persistent_backward_cut_round_on_two_unordered_streams(A):
+    """Two atomic persistent backward calls whose last rounds are cut into
+    pieces, in flight at once on two unordered streams (the end-to-end
+    leg's pattern).  Each call has its own workspace, its pieces' partial
+    slots and the conversion that sums them: dK and dV equal the same call
+    run alone bit for bit (the pieces are summed in a fixed order), dQ within
+    the gradient tolerance (atomic additions)."""
+    torch = G.torch_mod()
+    A.attn_set_bwd_persist(1)
+    try:
+        B, H, N, d = 4, 16, 1024, 128  # 512 units: 3 full rounds and a cut one (56 units in 2 pieces)
+        ta = G.inputs(B, H, N, d, d, seed=46)
+        tb = G.inputs(B, H, N, d, d, seed=47)
+        oa, la = G.run_fwd(A, ta, 0)
+        ob, lb = G.run_fwd(A, tb, 0)
+        ref_a = G.run_bwd(A, ta, oa, la, 0, 0)
+        ref_b = G.run_bwd(A, tb, ob, lb, 0, 0)
+        torch.cuda.synchronize()
+        G.check_status(A)
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        outs = []
+        for t, o, lse, s in ((ta, oa, la, s1), (tb, ob, lb, s2)):
+            grads = [torch.empty_like(t[n]) for n in ("q", "k", "v")]
+            nbytes = A.attn_bwd_workspace_bytes(B, H, N, d, d, 0)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+            outs.append((grads, ws, t, o, lse, s, nbytes))
+        torch.cuda.synchronize()
+        for _ in range(3):
+            for grads, ws, t, o, lse, s, nbytes in outs:
+                A.attn_bwd(t["q"], t["k"], t["v"], o, t["do"], lse, grads[0], grads[1], grads[2], B, H, N, d, d,
+                           0, 1.0 / math.sqrt(d), 0, ws, nbytes, s)
+        torch.cuda.synchronize()
+        G.check_status(A)
+        for (grads, *_), ref in zip(outs, (ref_a, ref_b)):
+            G.assert_grad_close("dq", G.f64(grads[0]), G.f64(ref[0]))
+            for got, want in zip(grads[1:], ref[1:]):
+                assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    finally:
+        A.attn_set_bwd_persist(-1)
+
+
 @pytest.mark.parametrize("group,desc", [(1, 0), (4, 1), (4, 0), (0, 1)])
 @pytest.mark.parametrize("causal", [0, 1])
 @pytest.mark.parametrize("persist", [0, 1])
