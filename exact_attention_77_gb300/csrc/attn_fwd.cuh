@@ -45,7 +45,11 @@ constexpr int kSubTile = 128 * 128;  // bytes: 128 rows x 128 B (one 128-byte sw
 constexpr int kPolyCols = 10;
 
 // ES: bytes per operand element (2: bf16; 1: e4m3).
-template <int DQK, int DV, int NQT, int ES = 2>
+// KS, VS: 0 for one K/V ring of kStages equal stages that K_j and V_j take in
+// turn; else KS stages sized for a K tile and VS for a V tile (K and V each
+// in their own ring) and no O staging tile (the instance must stage O in its
+// freed Q region).
+template <int DQK, int DV, int NQT, int ES = 2, int KS = 0, int VS = 0>
 struct FwdLayout {
   static constexpr int kQBytes = kTile * DQK * ES;
   static constexpr int kKBytes = kTile * DQK * ES;
@@ -60,13 +64,29 @@ struct FwdLayout {
   static constexpr int kQRegion = NQT * kQBytes;
   // Epilogue staging per query tile: one [128 rows x 64 columns] bf16 box of
   // O in the 128-byte swizzled layout the TMA store reads.
-  static constexpr int kStgBytes = kTile * 64 * 2;
+  static constexpr bool kSplitKV = KS > 0;
+  static constexpr int kKStages = KS, kVStages = VS;
+  static constexpr int kStgBytes = kSplitKV ? 0 : kTile * 64 * 2;
   // One query tile per CTA is sized so two CTAs share an SM (two softmax
   // warpgroups per SM either way); two tiles take the SM alone.
   static constexpr int kBudget = NQT == 1 ? 112 * 1024 : 226 * 1024;
   static constexpr int kStagesFit = (kBudget - kQRegion - NQT * kStgBytes) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
-  static_assert(kStages >= 2, "K/V ring needs two stages");
+  static constexpr int kStages = kSplitKV ? KS + VS : (kStagesFit > 4 ? 4 : kStagesFit);
+  static_assert(kSplitKV ? (KS >= 1 && VS >= 1) : kStages >= 2, "K/V ring needs two stages");
+  // Load ld of the K/V stream (even: K_j, odd: V_j; every unit starts on an
+  // even ld): its stage, the parity of that stage's use, and the stage's
+  // offset from kKVOff.
+  __host__ __device__ static constexpr int stage_of(int ld) {
+    return kSplitKV ? ((ld & 1) ? KS + (ld >> 1) % (VS > 0 ? VS : 1) : (ld >> 1) % (KS > 0 ? KS : 1))
+                    : ld % kStages;
+  }
+  __host__ __device__ static constexpr uint32_t phase_of(int ld) {
+    return (uint32_t)((kSplitKV ? ((ld & 1) ? (ld >> 1) / (VS > 0 ? VS : 1) : (ld >> 1) / (KS > 0 ? KS : 1))
+                                : ld / kStages) & 1);
+  }
+  __host__ __device__ static constexpr int stage_off(int st) {
+    return kSplitKV ? (st < KS ? st * kKBytes : KS * kKBytes + (st - KS) * kVBytes) : st * kStageBytes;
+  }
   static constexpr int kThreads = 128 + 128 * NQT;
   static constexpr int kMinBlocks = NQT == 1 ? 2 : 1;
   // Register split (setmaxnreg): the launch gives every thread kLaunchRegs;
@@ -77,7 +97,7 @@ struct FwdLayout {
   static constexpr int kSmRegs = NQT == 1 ? 208 : 208;
   static_assert(kCtlRegs * 128 + kSmRegs * 128 * NQT == kLaunchRegs * kThreads, "register split");
   static constexpr int kKVOff = kQRegion;
-  static constexpr int kStgOff = kKVOff + kStages * kStageBytes;
+  static constexpr int kStgOff = kKVOff + (kSplitKV ? KS * kKBytes + VS * kVBytes : kStages * kStageBytes);
   static constexpr int kBarOff = kStgOff + NQT * kStgBytes;
   static constexpr int kBarQFull = 0;
   static constexpr int kBarKVFull = 1;
@@ -120,7 +140,13 @@ template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool PERSIST, bool SP
           bool MASK = false>
 __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<DQK, DV, NQT>::kMinBlocks)
     fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = FwdLayout<DQK, DV, NQT, FP8 ? 1 : 2>;
+  // d_qk = 192 with one unit per CTA: two 48 KiB K stages and one 32 KiB V
+  // stage instead of two 48 KiB stages that K_j and V_j take in turn (O is
+  // staged in the freed Q region, so the staging tile's 32 KiB go to the
+  // second K stage).  Measured on GB300 against the shared ring: +5-6 % at
+  // N = 8192-16384, causal and not; one K and two V stages gave +1-2 %.
+  static constexpr bool kKV21 = DQK == 192 && !PERSIST && !SPLIT && !FP8 && !MASK;
+  using L = FwdLayout<DQK, DV, NQT, FP8 ? 1 : 2, kKV21 ? 2 : 0, kKV21 ? 1 : 0>;
   static_assert(!FP8 || (DQK == 128 && DV == 128 && !SPLIT), "FP8 instance: d = 128");
   static_assert(!MASK || (NQT == 1 && !CAUSAL && !SPLIT && !FP8), "masked instance: one query tile, no other mode");
   // (the FP8 instance is built with POLY = 0: the polynomial share measured
@@ -260,12 +286,12 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int ld = issued;
-            const int s = ld % L::kStages;
-            if (!mbar_wait(bar(L::kBarKVEmpty + s), ((ld / L::kStages) & 1) ^ 1, ctl, kWhereProdEmpty)) {
+            const int s = L::stage_of(ld);
+            if (!mbar_wait(bar(L::kBarKVEmpty + s), L::phase_of(ld) ^ 1, ctl, kWhereProdEmpty)) {
               ok = false;
               break;
             }
-            const uint32_t dst = sbase + L::kKVOff + s * L::kStageBytes;
+            const uint32_t dst = sbase + L::kKVOff + L::stage_off(s);
             ATTN_TRACE_AT(blockIdx.x, j, 13 + h);
             if (h == 0) {
               mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kKBytes);
@@ -286,8 +312,17 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       }
       // copies still in flight must land before the CTA can exit
       if (qn > 0) mbar_wait_drain(bar(L::kBarQFull), (qn - 1) & 1, p.timeout_ns);
-      for (int ld = issued > L::kStages ? issued - L::kStages : 0; ld < issued; ++ld)
-        mbar_wait_drain(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1, p.timeout_ns);
+      // (the last use of every stage: the last kStages loads of one ring, or
+      // the last KS K loads and VS V loads of split rings)
+      if constexpr (L::kSplitKV) {
+        for (int ld = issued > 2 * L::kKStages ? issued - 2 * L::kKStages : 0; ld < issued; ld += 2)  // K (issued is even)
+          mbar_wait_drain(bar(L::kBarKVFull + L::stage_of(ld)), L::phase_of(ld), p.timeout_ns);
+        for (int ld = issued > 2 * L::kVStages ? issued - 2 * L::kVStages + 1 : 1; ld < issued; ld += 2)  // V
+          mbar_wait_drain(bar(L::kBarKVFull + L::stage_of(ld)), L::phase_of(ld), p.timeout_ns);
+      } else {
+        for (int ld = issued > L::kStages ? issued - L::kStages : 0; ld < issued; ++ld)
+          mbar_wait_drain(bar(L::kBarKVFull + L::stage_of(ld)), L::phase_of(ld), p.timeout_ns);
+      }
     }
     __syncwarp();  // lanes 1-31 wait for lane 0 before the final barrier
   } else if (warp == 1) {
@@ -302,11 +337,11 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       return r;
     };
     auto wait_load = [&](int ld) -> bool {
-      return wait_all(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1, kWhereMmaKV);
+      return wait_all(bar(L::kBarKVFull + L::stage_of(ld)), L::phase_of(ld), kWhereMmaKV);
     };
     auto issue_qk = [&](int t, int stage) {
       const uint64_t da = sdesc_sw128(sbase + t * L::kQBytes, 16, 1024);
-      const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, 16, 1024);
+      const uint64_t db = sdesc_sw128(sbase + L::kKVOff + L::stage_off(stage), 16, 1024);
       if constexpr (!FP8) {  // statements of four products: one 64-column chunk each
         constexpr int kC = kSubTile / 16;
         static_assert(L::kQKSteps % 4 == 0 && L::kQKSteps <= 12, "K steps per S product");
@@ -323,7 +358,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       }
     };
     auto issue_pv = [&](int t, int stage, bool acc) {
-      const uint64_t db = sdesc_sw128(sbase + L::kKVOff + stage * L::kStageBytes, kSubTile, 1024);
+      const uint64_t db = sdesc_sw128(sbase + L::kKVOff + L::stage_off(stage), kSubTile, 1024);
       if constexpr (!FP8) {  // two statements of four products; A: P over 8 tensor-memory columns per step
         static_assert(L::kPVSteps == 8, "K steps per P V product");
         constexpr int kBS = L::kPVKeys * 128 / 16;
@@ -359,10 +394,10 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
 #pragma unroll
         for (int t = 0; t < NQT; ++t)
           if (w.nkv[t] > 0) {
-            issue_qk(t, ld0 % L::kStages);
+            issue_qk(t, L::stage_of(ld0));
             tc_commit_elect(bar(L::kBarSFull + t));
           }
-        tc_commit_elect(bar(L::kBarKVEmpty + ld0 % L::kStages));
+        tc_commit_elect(bar(L::kBarKVEmpty + L::stage_of(ld0)));
         // Q may be reloaded for the next unit once this unit's last S
         // products complete (here, or inside the loop below)
         if (PERSIST && w.nkv_max == 1) tc_commit_elect(bar(L::kBarQEmpty));
@@ -385,7 +420,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
         if (!(ok = wait_load(ldv))) break;
         if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 0);
         bool k_ready = false;
-        constexpr bool kEarlyV = L::kStages <= 2;
+        constexpr bool kEarlyV = L::kSplitKV || L::kStages <= 2;
         int last_pv = 0;  // the last tile whose P V product reads V_j
 #pragma unroll
         for (int t = 0; t < NQT; ++t)
@@ -396,7 +431,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
             ok = wait_all(bar(L::kBarPFull + t), pbit[t] ^ (j & 1), kWhereMmaP);
             if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 1 + 4 * t);
             if (ok) {
-              issue_pv(t, ldv % L::kStages, j > 0);
+              issue_pv(t, L::stage_of(ldv), j > 0);
               tc_commit_elect(bar(L::kBarODone + t));
               // With a two-stage ring (d_qk = 192) V_j's stage is released
               // as soon as its last P V product completes (the commit tracks
@@ -404,7 +439,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
               // V_{j+1} loads a product earlier: measured +10-12 % at 16K.
               // With four stages the later release is hidden, and the extra
               // commit between the products measured ~1 % slower.
-              if (kEarlyV && t == last_pv) tc_commit_elect(bar(L::kBarKVEmpty + ldv % L::kStages));
+              if (kEarlyV && t == last_pv) tc_commit_elect(bar(L::kBarKVEmpty + L::stage_of(ldv)));
               if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 2 + 4 * t);
             }
           }
@@ -414,7 +449,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
               if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 3);
             }
             if (ok) {
-              issue_qk(t, ldk % L::kStages);
+              issue_qk(t, L::stage_of(ldk));
               tc_commit_elect(bar(L::kBarSFull + t));
               if (lane == 0) ATTN_TRACE_AT(blockIdx.x, j, 4 + 4 * t);
             }
@@ -422,8 +457,8 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
         }
         if (!ok) break;
         if (PERSIST && j + 2 == w.nkv_max) tc_commit_elect(bar(L::kBarQEmpty));
-        if (!kEarlyV) tc_commit_elect(bar(L::kBarKVEmpty + ldv % L::kStages));
-        if (k_ready) tc_commit_elect(bar(L::kBarKVEmpty + ldk % L::kStages));
+        if (!kEarlyV) tc_commit_elect(bar(L::kBarKVEmpty + L::stage_of(ldv)));
+        if (k_ready) tc_commit_elect(bar(L::kBarKVEmpty + L::stage_of(ldk)));
       }
       if (!ok) break;
       if (PERSIST && w.nkv_max == 0) tc_commit_elect(bar(L::kBarQEmpty));
@@ -472,7 +507,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
       for (int ld = 0; live && ld < 2 * w0.nkv_max && ld / 2 < kTraceIters; ++ld) {
         int i = 0;
         for (; i < (1 << 22); ++i)
-          if (mbar_test(bar(L::kBarKVFull + ld % L::kStages), (ld / L::kStages) & 1)) break;
+          if (mbar_test(bar(L::kBarKVFull + L::stage_of(ld)), L::phase_of(ld))) break;
         live = i < (1 << 22);
         ATTN_TRACE_AT(blockIdx.x, ld / 2, 20 + (ld & 1));
       }
@@ -677,6 +712,7 @@ __global__ void __launch_bounds__(FwdLayout<DQK, DV, NQT>::kThreads, FwdLayout<D
           // last S product has completed) and, when it holds all of O's
           // boxes, takes them side by side: no box waits for another's store.
           constexpr bool kInQ = !PERSIST && L::kQBytes >= DV * kTile * 2;
+          static_assert(kInQ || !L::kSplitKV, "split K/V rings leave no O staging tile");
           constexpr uint32_t kBoxStride = kInQ ? kTile * 128 : 0;
           const uint32_t s_off = kInQ ? (uint32_t)(t * L::kQBytes) : (uint32_t)(L::kStgOff + t * L::kStgBytes);
           const int r_in = quad * 32 + lane;
@@ -749,6 +785,8 @@ cudaError_t launch_fwd_split_instance(const FwdParams& p, cudaStream_t stream) {
 template <int DQK, int DV, int NQT, bool CAUSAL, int POLY, bool FP8 = false, bool MASK = false>
 cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<DQK, DV, NQT, FP8 ? 1 : 2>;
+  constexpr bool kKV21 = DQK == 192 && !FP8 && !MASK;  // the one-unit-per-CTA instance's split rings
+  using L1 = FwdLayout<DQK, DV, NQT, FP8 ? 1 : 2, kKV21 ? 2 : 0, kKV21 ? 1 : 0>;
   // Persistent CTAs pay off when units are short (few K/V tiles each); with
   // long units the one-unit-per-CTA kernel is leaner and the launch order
   // already balances.  p.max_ctas > 0 forces the persistent grid.
@@ -758,14 +796,15 @@ cudaError_t launch_fwd_instance(const FwdParams& p, cudaStream_t stream) {
   // setmaxnreg.inc waits until the registers it asks for are free, so the
   // split must add up to what the launch actually hands out
   int sms = 0;
-  cudaError_t e = prepare_kernel((const void*)kernel, L::kSmemBytes, L::kLaunchRegs, &sms);
+  const int smem = persist ? L::kSmemBytes : L1::kSmemBytes;
+  cudaError_t e = prepare_kernel((const void*)kernel, smem, L::kLaunchRegs, &sms);
   if (e != cudaSuccess) return e;
   // persistent grid: as many CTAs as fit on the device at once, each looping
   // over work units (p.max_ctas > 0 sets the grid instead, e.g. one unit per
   // CTA when it is at least the number of units)
   int grid = !persist ? p.n_blocks : p.max_ctas > 0 ? p.max_ctas : sms * L::kMinBlocks;
   if (grid > p.n_blocks) grid = p.n_blocks;
-  kernel<<<grid, L::kThreads, L::kSmemBytes, stream>>>(p);
+  kernel<<<grid, L::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
