@@ -482,6 +482,37 @@ def test_deterministic_persistent_backward_on_two_unordered_streams(A):
         A.attn_set_bwd_persist(-1)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize(
+    "B,H,N",
+    [(1, 39, 512), (3, 17, 384), (1, 16, 1280), (2, 16, 600), (1, 20, 1024)],
+    ids=["s4", "rem1_s3", "s10_uneven", "s5_ragged", "s8"],
+)
+def test_persistent_backward_cut_round_piece_counts(A, d, B, H, N):
+    """More shapes whose last round is cut (one to ten pieces per unit, uneven
+    query-tile splits, a ragged N), both head sizes: every head's gradients
+    against the one-CTA-per-unit kernel, dK / dV bit-identical over repeats."""
+    torch = G.torch_mod()
+    t = G.inputs(B, H, N, d, d, seed=48)
+    o, lse = G.run_fwd(A, t, 0)
+    A.attn_set_bwd_persist(1)
+    try:
+        got = G.run_bwd(A, t, o, lse, 0, 0)
+        again = G.run_bwd(A, t, o, lse, 0, 0)
+        G.check_status(A)
+    finally:
+        A.attn_set_bwd_persist(0)
+    try:
+        one = G.run_bwd(A, t, o, lse, 0, 0)
+        G.check_status(A)
+    finally:
+        A.attn_set_bwd_persist(-1)
+    for name, x, y, z in zip(("dq", "dk", "dv"), got, one, again):
+        G.assert_grad_close(name, G.f64(x), G.f64(y))
+        if name != "dq":
+            assert torch.equal(x.view(torch.int16), z.view(torch.int16)), name
+
+
 def test_atomic_persistent_backward_cut_round_on_two_unordered_streams(A):
     """Two atomic persistent backward calls whose last rounds are cut into
     pieces, in flight at once on two unordered streams (the end-to-end
