@@ -218,6 +218,26 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def e2e_groups(BH: int, chunks: int, taper: bool) -> list:
+    """(first head, heads) of each head group of the end-to-end leg: ``chunks``
+    equal groups (fewer if they do not divide BH).  With ``taper`` the first
+    and last groups are halved, so the pipeline fills (the first group's
+    inputs going up before any kernel runs) and drains (the last group's
+    results coming down after the last kernel) with half as many bytes."""
+    n = max(1, min(chunks, BH))
+    while BH % n:
+        n -= 1
+    hc = BH // n
+    sizes = [hc] * n
+    if taper and hc >= 2 and n >= 2:
+        sizes = [hc // 2, hc - hc // 2] + [hc] * (n - 2) + [hc - hc // 2, hc // 2]
+    groups, h0 = [], 0
+    for sz in sizes:
+        groups.append((h0, sz))
+        h0 += sz
+    return groups
+
+
 def recorded_traffic(kernel: str, args):
     """DRAM bytes per launch from the committed ncu summary, if it still matches the sources."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -380,21 +400,9 @@ def run_ours(args, world, rank, local):
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
     d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
     BH = B * H
-    n_chunks = max(1, min(args.e2e_chunks, BH))
-    while BH % n_chunks:
-        n_chunks -= 1
-    hc = BH // n_chunks
-    # groups as (first head, heads); with --e2e-taper the first and last
-    # groups are halved, so the pipeline fills (the first group's inputs
-    # going up before any kernel runs) and drains (the last group's results
-    # coming down after the last kernel) with half as many bytes
-    sizes = [hc] * n_chunks
-    if args.e2e_taper and hc >= 2 and n_chunks >= 2:
-        sizes = [hc // 2, hc - hc // 2] + [hc] * (n_chunks - 2) + [hc - hc // 2, hc // 2]
-    groups, h0 = [], 0
-    for sz in sizes:
-        groups.append((h0, sz))
-        h0 += sz
+    groups = e2e_groups(BH, args.e2e_chunks, bool(args.e2e_taper))
+    sizes = [gn for _, gn in groups]
+    hc = max(sizes)
     n_chunks = len(groups)
     flat = lambda x: x.reshape(BH, *x.shape[2:])
     # the forward needs Q, K, V only, and O / LSE are final once it has run:

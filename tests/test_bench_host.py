@@ -89,3 +89,21 @@ def test_roofline_peak_is_burst_unless_power_capped():
     assert p == 1698.1 and "power cap" in note
     p, _ = bench.roofline_peak({}, {"reasons": None})
     assert p == bench.FALLBACK_PEAKS["bf16_tflops"]
+
+
+def test_e2e_groups_cover_every_head_once():
+    for BH, chunks in ((16, 8), (16, 16), (16, 4), (12, 8), (1, 8), (7, 3)):
+        for taper in (False, True):
+            groups = bench.e2e_groups(BH, chunks, taper)
+            heads = [h for g0, gn in groups for h in range(g0, g0 + gn)]
+            assert heads == list(range(BH)), (BH, chunks, taper)
+            assert all(gn >= 1 for _, gn in groups)
+
+
+def test_e2e_groups_taper_halves_the_ends():
+    assert [gn for _, gn in bench.e2e_groups(16, 8, False)] == [2] * 8
+    assert [gn for _, gn in bench.e2e_groups(16, 8, True)] == [1, 1, 2, 2, 2, 2, 2, 2, 1, 1]
+    assert [gn for _, gn in bench.e2e_groups(16, 4, True)] == [2, 2, 4, 4, 2, 2]
+    # one-head groups cannot be halved; a single group is not tapered
+    assert [gn for _, gn in bench.e2e_groups(16, 16, True)] == [1] * 16
+    assert [gn for _, gn in bench.e2e_groups(16, 1, True)] == [16]
