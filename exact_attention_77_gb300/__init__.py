@@ -39,6 +39,7 @@ _SIGS = {
     "attn_set_rescale_counter": (_I, [_P]),
     "attn_set_rescale_threshold": (_I, [_F]),
     "attn_set_bwd_pair": (_I, [_I]),
+    "attn_set_fwd_persist": (_I, [_I]),
     "attn_set_bwd_persist": (_I, [_I]),
     "attn_set_exp_poly": (_I, [_I]),
     "attn_set_det_schedule": (_I, [_I, _I]),
@@ -289,6 +290,10 @@ def attn_set_rescale_threshold(tau: float):
 
 def attn_set_bwd_pair(enable: int):
     _check(get_lib().attn_set_bwd_pair(int(enable)))
+
+
+def attn_set_fwd_persist(mode: int):
+    _check(get_lib().attn_set_fwd_persist(int(mode)))
 
 
 def attn_set_bwd_persist(mode: int):

@@ -348,6 +348,14 @@ int attn_set_bwd_pair(int enable) {
   return ATTN_OK;
 }
 
+int attn_set_fwd_persist(int mode) {
+  if (mode < -1 || mode > 1) return ATTN_ERR_INVALID_ARG;
+  settings();
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_settings.fwd_persist = mode;
+  return ATTN_OK;
+}
+
 int attn_set_bwd_persist(int mode) {
   if (mode < -1 || mode > 1) return ATTN_ERR_INVALID_ARG;
   settings();

@@ -369,6 +369,17 @@ int attn_set_exp_poly(int enable);
 int attn_set_bwd_pair(int enable);
 
 /*
+ * Forward kernel selection for later attn_fwd, attn_fwd_gqa, attn_fwd_fp8 and
+ * attn_fwd_masked calls: mode = 1 runs the persistent kernel (as many CTAs as
+ * fit on the GPU at once, each taking units of query tiles in turn), 0 one
+ * CTA per unit, -1 (the default; also ATTN_FWD_PERSIST at first use) chooses
+ * by size: persistent for N <= 2048, causal N <= 4096, and windows short
+ * enough to make units short (attn_fwd_masked).  Results meet the same
+ * tolerances either way.  Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
+ */
+int attn_set_fwd_persist(int mode);
+
+/*
  * Backward main kernel selection for later attn_bwd / attn_bwd_noalloc calls:
  * mode = 1 runs the persistent kernel (one CTA per SM taking the (head, key
  * tile) units in rounds), 0 the kernel with one CTA per unit, -1 (the

@@ -135,6 +135,10 @@ def test_tuning_setters(lib):
     assert lib.get_lib().attn_set_bwd_persist(-2) == A.ATTN_ERR_INVALID_ARG
     for m in (1, 0, -1):
         assert lib.get_lib().attn_set_bwd_persist(m) == A.ATTN_OK
+    assert lib.get_lib().attn_set_fwd_persist(2) == A.ATTN_ERR_INVALID_ARG
+    assert lib.get_lib().attn_set_fwd_persist(-2) == A.ATTN_ERR_INVALID_ARG
+    for m in (1, 0, -1):
+        assert lib.get_lib().attn_set_fwd_persist(m) == A.ATTN_OK
     assert lib.get_lib().attn_set_exp_poly(2) == A.ATTN_ERR_INVALID_ARG
     assert lib.get_lib().attn_set_exp_poly(-1) == A.ATTN_ERR_INVALID_ARG
     assert lib.get_lib().attn_set_exp_poly(1) == A.ATTN_OK

@@ -65,6 +65,21 @@ def test_forward_ragged_and_small(A, dqk, dv, N, causal):
     _full_fwd_check(A, 1, 3, N, dqk, dv, bool(causal))
 
 
+@pytest.mark.parametrize("persist", [0, 1], ids=["one_unit_per_cta", "persistent"])
+@pytest.mark.parametrize("dqk,dv", [(64, 64), (128, 128), (192, 128)])
+@pytest.mark.parametrize("N", [1, 300, 1000])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_forward_both_kernels(A, persist, dqk, dv, N, causal):
+    """The persistent and the one-CTA-per-unit forward, each forced, on small
+    and ragged sizes with several units (the latter is otherwise chosen only
+    for long sequences; at d_qk = 192 it runs K and V in rings of their own)."""
+    A.attn_set_fwd_persist(persist)
+    try:
+        _full_fwd_check(A, 2, 3, N, dqk, dv, bool(causal))
+    finally:
+        A.attn_set_fwd_persist(-1)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [1, 100, 128, 257, 384])
 @pytest.mark.parametrize("causal", [0, 1])
